@@ -1,0 +1,286 @@
+"""Python binding of the DLRM sparse-path C ABI (libdlrm_sparse.so, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  torch tensors provide device memory and streams.
+The functions carry the names of the C entry points declared in
+include/dlrm_sparse.h; see that header for layouts and semantics.
+
+There is no fallback: if the CUDA library is missing or was not built, every
+call raises RuntimeError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdlrm_sparse.so")
+
+DLRM_OK = 0
+DLRM_ERR_INVALID_ARG = 1
+DLRM_ERR_INDEX_OOB = 2
+DLRM_ERR_BAD_OFFSETS = 4
+DLRM_ERR_TIMEOUT = 8
+DLRM_ERR_CUDA = 16
+DLRM_ERR_UNSUPPORTED = 32
+MAX_TABLES = 128
+
+_MODES = {"sum": 0, "mean": 1}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+_ITYPES = {torch.int32: 0, torch.int64: 1}
+
+C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sparse_fwd_host",
+             "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_status_string",
+             "dlrm_abi_version")
+
+
+class DlrmTables(ctypes.Structure):
+    _fields_ = [("num_tables", ctypes.c_int32), ("dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("data", ctypes.POINTER(ctypes.c_void_p)), ("num_rows", ctypes.POINTER(ctypes.c_int64))]
+
+
+class DlrmBags(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("nnz", ctypes.c_int64), ("index_type", ctypes.c_int32),
+                ("indices", ctypes.c_void_p), ("offsets", ctypes.c_void_p)]
+
+
+class DlrmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdlrm_sparse.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} not found: build it with embedding_bag_lookup_dlrm_b300/build.py "
+                           "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P, T, B = ctypes.c_void_p, ctypes.POINTER(DlrmTables), ctypes.POINTER(DlrmBags)
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "dlrm_embbag_fwd": ([T, B, i32, P, P, P], i32),
+        "dlrm_interact_fwd": ([P, P, i64, i32, i32, P, P], i32),
+        "dlrm_sparse_fwd": ([T, B, i32, P, P, P, P, P], i32),
+        "dlrm_sparse_fwd_host": ([T, B, i32, P, P, P, P, P, P, P, P], i32),
+        "dlrm_sparse_bwd_workspace_size": ([T, B, ctypes.POINTER(ctypes.c_size_t)], i32),
+        "dlrm_sparse_bwd_adagrad": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p), ctypes.c_float,
+                                     ctypes.c_float, P, ctypes.c_size_t, P, P], i32),
+        "dlrm_status_string": ([i32], ctypes.c_char_p),
+        "dlrm_abi_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().dlrm_status_string(status).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check_cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+class Tables:
+    """A C view (dlrm_tables) of a list of 2-D CUDA tensors of equal width and dtype."""
+
+    def __init__(self, tables):
+        tables = list(tables)
+        if not tables:
+            raise ValueError("need at least one table")
+        D, dt = tables[0].shape[1], tables[0].dtype
+        for i, t in enumerate(tables):
+            _check_cuda(t, f"tables[{i}]")
+            if t.dim() != 2 or t.shape[1] != D or t.dtype != dt:
+                raise ValueError("tables must be 2-D with equal width and dtype")
+        if dt not in _DTYPES:
+            raise ValueError(f"unsupported table dtype {dt}")
+        self.tensors = tables
+        self._ptrs = (ctypes.c_void_p * len(tables))(*[t.data_ptr() for t in tables])
+        self._rows = (ctypes.c_int64 * len(tables))(*[t.shape[0] for t in tables])
+        self.c = DlrmTables(len(tables), D, _DTYPES[dt], self._ptrs, self._rows)
+        self.T, self.D = len(tables), D
+
+
+def _bags(indices, offsets, B, device=True) -> DlrmBags:
+    if indices.dtype != offsets.dtype or indices.dtype not in _ITYPES:
+        raise ValueError("indices and offsets must share dtype int32 or int64")
+    if device:
+        _check_cuda(indices, "indices")
+        _check_cuda(offsets, "offsets")
+    return DlrmBags(B, indices.numel(), _ITYPES[indices.dtype], indices.data_ptr() if indices.numel() else None,
+                    offsets.data_ptr())
+
+
+def _batch(offsets, T):
+    n = offsets.numel() - 1
+    if n < T or n % T:
+        raise ValueError(f"offsets must hold T*B+1 entries (T={T}), got {offsets.numel()}")
+    return n // T
+
+
+def _raise(st, where):
+    if st != DLRM_OK:
+        raise DlrmError(st, where)
+
+
+def _tables(tables):
+    return tables if isinstance(tables, Tables) else Tables(tables)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def dlrm_embbag_fwd(tables, indices, offsets, mode="sum", pooled=None, status=None, stream=None):
+    """Pooled embeddings [B, T, D] fp32 of CSR bags (table-major offsets of T*B+1 entries)."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    if pooled is None:
+        pooled = torch.empty((B, tb.T, tb.D), dtype=torch.float32, device=indices.device)
+    _check_cuda(pooled, "pooled", torch.float32)
+    bags = _bags(indices, offsets, B)
+    st = lib.dlrm_embbag_fwd(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], pooled.data_ptr(),
+                             status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _raise(st, "dlrm_embbag_fwd")
+    return pooled
+
+
+def dlrm_interact_fwd(dense, pooled, out=None, stream=None):
+    """[x, strict upper triangle of V V^T] per sample, V = [x; pooled]."""
+    lib = load_library()
+    _check_cuda(dense, "dense", torch.float32)
+    _check_cuda(pooled, "pooled", torch.float32)
+    B, T, D = pooled.shape
+    N = T + 1
+    if out is None:
+        out = torch.empty((B, D + N * (N - 1) // 2), dtype=torch.float32, device=dense.device)
+    _check_cuda(out, "out", torch.float32)
+    st = lib.dlrm_interact_fwd(dense.data_ptr(), pooled.data_ptr(), B, T, D, out.data_ptr(), _stream_ptr(stream))
+    _raise(st, "dlrm_interact_fwd")
+    return out
+
+
+def dlrm_sparse_fwd(tables, indices, offsets, dense, mode="sum", out=None, pooled_save=None, status=None,
+                    stream=None):
+    """Fused lookup + pooling + interaction: out [B, D + N(N-1)/2] fp32."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    _check_cuda(dense, "dense", torch.float32)
+    N = tb.T + 1
+    if out is None:
+        out = torch.empty((B, tb.D + N * (N - 1) // 2), dtype=torch.float32, device=dense.device)
+    _check_cuda(out, "out", torch.float32)
+    if pooled_save is not None:
+        _check_cuda(pooled_save, "pooled_save", torch.float32)
+    bags = _bags(indices, offsets, B)
+    st = lib.dlrm_sparse_fwd(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
+                             out.data_ptr(), pooled_save.data_ptr() if pooled_save is not None else None,
+                             status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _raise(st, "dlrm_sparse_fwd")
+    return out
+
+
+class HostStaging:
+    """Device staging buffers for dlrm_sparse_fwd_host (allocated once by the caller)."""
+
+    def __init__(self, B, T, D, nnz, index_dtype=torch.int32, device="cuda"):
+        N = T + 1
+        self.indices = torch.empty(max(nnz, 1), dtype=index_dtype, device=device)
+        self.offsets = torch.empty(T * B + 1, dtype=index_dtype, device=device)
+        self.dense = torch.empty((B, D), dtype=torch.float32, device=device)
+        self.out = torch.empty((B, D + N * (N - 1) // 2), dtype=torch.float32, device=device)
+
+
+def dlrm_sparse_fwd_host(tables, indices_host, offsets_host, dense_host, out_host, staging: HostStaging,
+                         mode="sum", status=None, stream=None):
+    """The fused forward fed from host (ideally pinned) tensors; the copies and the
+    kernel are queued on `stream`; out_host is valid after the stream syncs."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets_host, tb.T)
+    for name, t in (("indices_host", indices_host), ("offsets_host", offsets_host), ("dense_host", dense_host),
+                    ("out_host", out_host)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if staging.indices.numel() < indices_host.numel() or staging.offsets.numel() < offsets_host.numel():
+        raise ValueError("staging buffers too small")
+    bags = _bags(indices_host, offsets_host, B, device=False)
+    st = lib.dlrm_sparse_fwd_host(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense_host.data_ptr(),
+                                  out_host.data_ptr(), staging.indices.data_ptr(), staging.offsets.data_ptr(),
+                                  staging.dense.data_ptr(), staging.out.data_ptr(),
+                                  status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _raise(st, "dlrm_sparse_fwd_host")
+    return out_host
+
+
+def dlrm_sparse_bwd_workspace_size(tables, indices, offsets) -> int:
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    bags = _bags(indices, offsets, B, device=False)
+    n = ctypes.c_size_t(0)
+    _raise(lib.dlrm_sparse_bwd_workspace_size(ctypes.byref(tb.c), ctypes.byref(bags), ctypes.byref(n)),
+           "dlrm_sparse_bwd_workspace_size")
+    return int(n.value)
+
+
+def dlrm_sparse_bwd_adagrad(tables, accum, indices, offsets, dense, pooled_saved, grad_out, lr, eps, mode="sum",
+                            grad_dense=None, workspace=None, status=None, stream=None):
+    """One training step of the sparse path; tables and accum are updated in place.
+    Returns grad_dense [B, D]."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    if len(accum) != tb.T:
+        raise ValueError("one accumulator per table")
+    for i, a in enumerate(accum):
+        _check_cuda(a, f"accum[{i}]", torch.float32)
+        if a.numel() != tb.tensors[i].shape[0]:
+            raise ValueError(f"accum[{i}] must hold one value per row")
+    for name, t in (("dense", dense), ("pooled_saved", pooled_saved), ("grad_out", grad_out)):
+        _check_cuda(t, name, torch.float32)
+    if grad_dense is None:
+        grad_dense = torch.empty((B, tb.D), dtype=torch.float32, device=dense.device)
+    _check_cuda(grad_dense, "grad_dense", torch.float32)
+    need = dlrm_sparse_bwd_workspace_size(tb, indices, offsets)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dense.device)
+    _check_cuda(workspace, "workspace")
+    acc_ptrs = (ctypes.c_void_p * tb.T)(*[a.data_ptr() for a in accum])
+    bags = _bags(indices, offsets, B)
+    st = lib.dlrm_sparse_bwd_adagrad(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
+                                     pooled_saved.data_ptr(), grad_out.data_ptr(), grad_dense.data_ptr(), acc_ptrs,
+                                     float(lr), float(eps), workspace.data_ptr(), workspace.numel(),
+                                     status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _raise(st, "dlrm_sparse_bwd_adagrad")
+    return grad_dense

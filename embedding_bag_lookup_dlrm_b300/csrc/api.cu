@@ -1,0 +1,223 @@
+// api.cu -- the C ABI declared in include/dlrm_sparse.h: host-side argument
+// checks, packing of the kernel parameter blocks, launches.  Nothing here
+// allocates device memory or touches data on the host.
+#include <stdint.h>
+#include <string.h>
+
+#include "dlrm_sparse.h"
+#include "internal.h"
+
+namespace {
+
+using dlrm::BwdArgs;
+using dlrm::FwdArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_supported(int32_t D) { return D == 16 || D == 32 || D == 64 || D == 128 || D == 256; }
+
+dlrm_status check_tables(const dlrm_tables* t)
+{
+    if (t == nullptr || t->data == nullptr || t->num_rows == nullptr) return DLRM_ERR_INVALID_ARG;
+    if (t->num_tables < 1 || t->num_tables > DLRM_MAX_TABLES) return DLRM_ERR_INVALID_ARG;
+    if (t->dtype != DLRM_F32 && t->dtype != DLRM_BF16) return DLRM_ERR_INVALID_ARG;
+    if (t->dim <= 0 || t->dim > 256 || t->dim % 4 != 0) return DLRM_ERR_INVALID_ARG;
+    if (!dim_supported(t->dim)) return DLRM_ERR_UNSUPPORTED;
+    for (int i = 0; i < t->num_tables; ++i) {
+        if (t->data[i] == nullptr || !aligned16(t->data[i])) return DLRM_ERR_INVALID_ARG;
+        if (t->num_rows[i] < 1) return DLRM_ERR_INVALID_ARG;
+    }
+    return DLRM_OK;
+}
+
+dlrm_status check_bags(const dlrm_bags* b, int32_t T)
+{
+    if (b == nullptr || b->batch < 1 || b->nnz < 0) return DLRM_ERR_INVALID_ARG;
+    if (b->index_type != DLRM_I32 && b->index_type != DLRM_I64) return DLRM_ERR_INVALID_ARG;
+    if (b->offsets == nullptr || (b->nnz > 0 && b->indices == nullptr)) return DLRM_ERR_INVALID_ARG;
+    if (b->batch > (int64_t{1} << 40) / T) return DLRM_ERR_INVALID_ARG;
+    if (b->index_type == DLRM_I32 && (b->nnz > INT32_MAX || int64_t{T} * b->batch + 1 > INT32_MAX))
+        return DLRM_ERR_INVALID_ARG;
+    return DLRM_OK;
+}
+
+bool mode_ok(dlrm_pool_mode m) { return m == DLRM_POOL_SUM || m == DLRM_POOL_MEAN; }
+
+void pack_forward(FwdArgs& a, const dlrm_tables* t, const dlrm_bags* b, dlrm_pool_mode mode)
+{
+    memset(&a, 0, sizeof a);
+    for (int i = 0; i < t->num_tables; ++i) {
+        a.tables[i] = t->data[i];
+        a.num_rows[i] = t->num_rows[i];
+    }
+    a.indices = b->indices;
+    a.offsets = b->offsets;
+    a.B = b->batch;
+    a.nnz = b->nnz;
+    a.T = t->num_tables;
+    a.mean = mode == DLRM_POOL_MEAN;
+}
+
+int64_t out_width(int32_t T, int32_t D) { return D + int64_t{T + 1} * T / 2; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t dlrm_abi_version(void) { return 1; }
+
+const char* dlrm_status_string(dlrm_status s)
+{
+    if (s == DLRM_OK) return "ok";
+    if (s & DLRM_ERR_INVALID_ARG) return "invalid argument";
+    if (s & DLRM_ERR_INDEX_OOB) return "index out of range";
+    if (s & DLRM_ERR_BAD_OFFSETS) return "malformed offsets";
+    if (s & DLRM_ERR_TIMEOUT) return "device wait timed out";
+    if (s & DLRM_ERR_CUDA) return "CUDA error";
+    if (s & DLRM_ERR_UNSUPPORTED) return "unsupported configuration";
+    return "unknown status";
+}
+
+dlrm_status dlrm_embbag_fwd(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode, float* pooled,
+                            int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (!mode_ok(mode) || pooled == nullptr || !aligned16(pooled)) return DLRM_ERR_INVALID_ARG;
+    FwdArgs a;
+    pack_forward(a, tables, bags, mode);
+    a.pooled_out = pooled;
+    a.status = status_dev;
+    return dlrm::launch_forward(dlrm::kEmbbag, a, tables->dim, tables->dtype, bags->index_type, stream);
+}
+
+dlrm_status dlrm_interact_fwd(const float* dense, const float* pooled, int64_t batch, int32_t num_tables, int32_t dim,
+                              float* out, cudaStream_t stream)
+{
+    if (dense == nullptr || pooled == nullptr || out == nullptr) return DLRM_ERR_INVALID_ARG;
+    if (!aligned16(dense) || !aligned16(pooled) || (reinterpret_cast<uintptr_t>(out) & 3u)) return DLRM_ERR_INVALID_ARG;
+    if (batch < 1 || num_tables < 1 || num_tables > DLRM_MAX_TABLES) return DLRM_ERR_INVALID_ARG;
+    if (dim <= 0 || dim > 256 || dim % 4 != 0) return DLRM_ERR_INVALID_ARG;
+    if (!dim_supported(dim)) return DLRM_ERR_UNSUPPORTED;
+    FwdArgs a;
+    memset(&a, 0, sizeof a);
+    a.dense = dense;
+    a.pooled_in = pooled;
+    a.out = out;
+    a.B = batch;
+    a.T = num_tables;
+    return dlrm::launch_forward(dlrm::kInteract, a, dim, DLRM_F32, DLRM_I32, stream);
+}
+
+dlrm_status dlrm_sparse_fwd(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode, const float* dense,
+                            float* out, float* pooled_save, int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (!mode_ok(mode) || dense == nullptr || out == nullptr || !aligned16(dense)) return DLRM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(out) & 3u) return DLRM_ERR_INVALID_ARG;
+    if (pooled_save != nullptr && !aligned16(pooled_save)) return DLRM_ERR_INVALID_ARG;
+    FwdArgs a;
+    pack_forward(a, tables, bags, mode);
+    a.dense = dense;
+    a.out = out;
+    a.pooled_out = pooled_save;
+    a.status = status_dev;
+    return dlrm::launch_forward(dlrm::kFused, a, tables->dim, tables->dtype, bags->index_type, stream);
+}
+
+dlrm_status dlrm_sparse_fwd_host(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                 const float* dense_host, float* out_host, void* indices_dev, void* offsets_dev,
+                                 float* dense_dev, float* out_dev, int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (dense_host == nullptr || out_host == nullptr || offsets_dev == nullptr || dense_dev == nullptr ||
+        out_dev == nullptr || (bags->nnz > 0 && indices_dev == nullptr))
+        return DLRM_ERR_INVALID_ARG;
+    const size_t isz = bags->index_type == DLRM_I32 ? 4 : 8;
+    const int64_t B = bags->batch, T = tables->num_tables, D = tables->dim;
+    if (bags->nnz > 0 &&
+        cudaMemcpyAsync(indices_dev, bags->indices, bags->nnz * isz, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    if (cudaMemcpyAsync(offsets_dev, bags->offsets, (T * B + 1) * isz, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return DLRM_ERR_CUDA;
+    if (cudaMemcpyAsync(dense_dev, dense_host, B * D * sizeof(float), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    dlrm_bags dev = *bags;
+    dev.indices = indices_dev;
+    dev.offsets = offsets_dev;
+    st = dlrm_sparse_fwd(tables, &dev, mode, dense_dev, out_dev, nullptr, status_dev, stream);
+    if (st != DLRM_OK) return st;
+    const size_t out_bytes = static_cast<size_t>(B) * out_width(tables->num_tables, tables->dim) * sizeof(float);
+    if (cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    return DLRM_OK;
+}
+
+dlrm_status dlrm_sparse_bwd_workspace_size(const dlrm_tables* tables, const dlrm_bags* bags, size_t* bytes)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (bytes == nullptr) return DLRM_ERR_INVALID_ARG;
+    *bytes = dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz);
+    return DLRM_OK;
+}
+
+dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                    const float* dense, const float* pooled_saved, const float* grad_out,
+                                    float* grad_dense, float* const* accum, float lr, float eps, void* workspace,
+                                    size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (tables->dtype != DLRM_F32) return DLRM_ERR_UNSUPPORTED;
+    if (!mode_ok(mode) || dense == nullptr || pooled_saved == nullptr || grad_out == nullptr ||
+        grad_dense == nullptr || accum == nullptr || workspace == nullptr)
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned16(dense) || !aligned16(pooled_saved) || !aligned16(grad_dense) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(grad_out) & 3u))
+        return DLRM_ERR_INVALID_ARG;
+    const int64_t total_rows = [&] {
+        int64_t s = 0;
+        for (int i = 0; i < tables->num_tables; ++i) s += tables->num_rows[i];
+        return s;
+    }();
+    if (total_rows >= (int64_t{1} << 32) - 1) return DLRM_ERR_UNSUPPORTED;  // sort keys are 32-bit
+    if (workspace_bytes < dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz))
+        return DLRM_ERR_INVALID_ARG;
+    BwdArgs a;
+    memset(&a, 0, sizeof a);
+    int64_t base = 0;
+    for (int i = 0; i < tables->num_tables; ++i) {
+        if (accum[i] == nullptr || !aligned16(accum[i])) return DLRM_ERR_INVALID_ARG;
+        a.tables[i] = static_cast<float*>(tables->data[i]);
+        a.accum[i] = accum[i];
+        a.num_rows[i] = tables->num_rows[i];
+        a.row_base[i] = base;
+        base += tables->num_rows[i];
+    }
+    a.row_base[tables->num_tables] = base;
+    a.indices = bags->indices;
+    a.offsets = bags->offsets;
+    a.dense = dense;
+    a.pooled = pooled_saved;
+    a.grad_out = grad_out;
+    a.grad_dense = grad_dense;
+    a.status = status_dev;
+    a.B = bags->batch;
+    a.nnz = bags->nnz;
+    a.T = tables->num_tables;
+    a.mean = mode == DLRM_POOL_MEAN;
+    a.lr = lr;
+    a.eps = eps;
+    return dlrm::launch_backward(a, tables->dim, bags->index_type, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"

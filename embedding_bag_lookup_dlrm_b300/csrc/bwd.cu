@@ -1,0 +1,667 @@
+// bwd.cu -- sm_103a kernels of the DLRM sparse training step:
+//   interaction backward -> lookup keys -> stable LSD radix sort by row ->
+//   ordered segment sums -> row-wise Adagrad, in place.
+//
+// Training with Adagrad: "DLRM" (robocikowo.com), "Forward pass", last
+// sentence.  The backward of out = [x, triu(V V^T)] is calculus on steps
+// (3)-(4) of the same paragraph:  dV_i = sum_{j != i} g(i,j) V_j with
+// g(i,j) = g(j,i) the upstream gradient of pair (i,j).
+//
+// Reproducibility: every floating-point sum here runs in an order fixed by
+// the data layout alone (the stable sort keeps lookups of a row in lookup
+// order; long runs are cut into fixed-size chunks whose partial sums are
+// added in chunk order), so two calls on the same inputs give the same bits.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dlrm {
+namespace {
+
+constexpr uint32_t kSentinel = 0xFFFFFFFFu;  // key of a lookup that updates nothing
+
+// ---- workspace layout ------------------------------------------------------
+constexpr int kSortThreads = 256;
+constexpr int kSortItems = 16;
+constexpr int kSortTile = kSortThreads * kSortItems;  // 4096 keys per tile
+constexpr int kRadixBits = 8;
+constexpr int kBins = 1 << kRadixBits;
+constexpr int kChunk = 256;  // sorted lookups per segment-reduction warp
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
+
+struct Workspace {
+    float* dP;          // B x T x D
+    uint32_t* keys[2];  // nnz each, ping-pong
+    uint32_t* vals[2];
+    uint32_t* counts;   // kBins x num_tiles
+    uint32_t* bin_total;  // kBins
+    float* partial;     // 2 x num_chunks x D
+    int64_t num_tiles, num_chunks;
+};
+
+Workspace carve(void* base, int64_t B, int32_t T, int32_t D, int64_t nnz, size_t* total)
+{
+    Workspace w{};
+    w.num_tiles = (nnz + kSortTile - 1) / kSortTile;
+    w.num_chunks = (nnz + kChunk - 1) / kChunk;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    const size_t o_dP = take(sizeof(float) * B * T * D);
+    size_t o_k[2], o_v[2];
+    for (int i = 0; i < 2; ++i) {
+        o_k[i] = take(sizeof(uint32_t) * nnz);
+        o_v[i] = take(sizeof(uint32_t) * nnz);
+    }
+    const size_t o_cnt = take(sizeof(uint32_t) * kBins * (w.num_tiles > 0 ? w.num_tiles : 1));
+    const size_t o_tot = take(sizeof(uint32_t) * kBins);
+    const size_t o_par = take(sizeof(float) * 2 * (w.num_chunks > 0 ? w.num_chunks : 1) * D);
+    if (total) *total = o;
+    if (base) {
+        char* p = static_cast<char*>(base);
+        w.dP = reinterpret_cast<float*>(p + o_dP);
+        for (int i = 0; i < 2; ++i) {
+            w.keys[i] = reinterpret_cast<uint32_t*>(p + o_k[i]);
+            w.vals[i] = reinterpret_cast<uint32_t*>(p + o_v[i]);
+        }
+        w.counts = reinterpret_cast<uint32_t*>(p + o_cnt);
+        w.bin_total = reinterpret_cast<uint32_t*>(p + o_tot);
+        w.partial = reinterpret_cast<float*>(p + o_par);
+    }
+    return w;
+}
+
+template <typename TI>
+__device__ __forceinline__ int64_t ld_index(const void* p, int64_t i)
+{
+    return static_cast<int64_t>(__ldg(static_cast<const TI*>(p) + i));
+}
+
+// ---------------------------------------------------------------------------
+// 1. Interaction backward.  One group of G warps per sample.  V (x, then the
+// pooled rows) arrives by two bulk copies; the symmetric upstream matrix g
+// (zero diagonal) is built in shared memory from the triangle.  Each lane owns
+// 16-byte column chunks of V and accumulates an 8-row block of dV = g V.
+// ---------------------------------------------------------------------------
+struct BwdLayout {
+    int N, NP, K;  // NP = N rounded up to 8 (rows of g)
+    int off_V, off_g, off_tri, bytes;
+};
+
+__host__ __device__ inline BwdLayout make_bwd_layout(int T, int D)
+{
+    BwdLayout l;
+    l.N = T + 1;
+    l.NP = round_up(l.N, 8);
+    l.K = l.N * (l.N - 1) / 2;
+    int o = 16;  // mbarrier
+    l.off_V = o;
+    o += 4 * l.N * D;
+    l.off_g = o;
+    o += 4 * l.NP * l.NP;
+    l.off_tri = o;
+    o += 4 * l.K;
+    l.bytes = round_up(o, 128);
+    return l;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant__ BwdArgs a, float* __restrict__ dP,
+                                                           int groups_per_cta)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int GT = G * kWarp;
+    constexpr int CPR = D / 4;                       // float4 chunks per row
+    constexpr int LPR = CPR < kWarp ? CPR : kWarp;   // lanes per row
+    constexpr int CPL = CPR / LPR;                   // chunks per lane
+    constexpr int RPI = kWarp / LPR;                 // row blocks worked on side by side
+    const BwdLayout l = make_bwd_layout(a.T, D);
+    const int group = threadIdx.x / GT;
+    const int gl = threadIdx.x % GT;
+    const int lane = gl % kWarp;
+    const int wig = gl / kWarp;
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * groups_per_cta + group;
+    if (b >= a.B) return;
+
+    unsigned char* base = smem + group * l.bytes;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(base);
+    float* V = reinterpret_cast<float*>(base + l.off_V);
+    float* gm = reinterpret_cast<float*>(base + l.off_g);
+    float* tri = reinterpret_cast<float*>(base + l.off_tri);
+    const int T = a.T, N = l.N, NP = l.NP, K = l.K;
+    const int W = D + K;
+
+    if (gl == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (G == 1) __syncwarp(); else __syncthreads();
+    if (gl == 0) {
+        const uint32_t xb = D * 4, pb = static_cast<uint32_t>(T) * D * 4;
+        mbar_arrive_expect_tx(bar, xb + pb);
+        bulk_g2s(V, a.dense + b * D, xb, bar);
+        bulk_g2s(V + D, a.pooled + b * T * D, pb, bar);
+    }
+    const float* go = a.grad_out + b * W;
+    for (int k = gl; k < K; k += GT) tri[k] = go[D + k];
+    if (G == 1) __syncwarp(); else __syncthreads();
+    for (int e = gl; e < NP * NP; e += GT) {
+        const int i = e / NP, j = e - (e / NP) * NP;
+        float v = 0.0f;
+        if (i < N && j < N && i != j) v = tri[i < j ? tri_index(i, j, N) : tri_index(j, i, N)];
+        gm[e] = v;
+    }
+    const bool landed = mbar_wait_bounded(bar, 0);
+    const bool failed = (G == 1) ? (__any_sync(0xffffffffu, !landed) != 0) : (__syncthreads_or(!landed) != 0);
+    if (failed) {
+        if (gl == 0) flag_status(a.status, DLRM_ERR_TIMEOUT);
+        return;
+    }
+    if (G == 1) __syncwarp();
+
+    const int h = lane / LPR;            // row-block lane set
+    const int c0 = lane % LPR;
+    const int nblk = NP / 8;
+    for (int ib = wig * RPI + h; ib < nblk; ib += G * RPI) {
+        const int i0 = ib * 8;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int col = (c0 + k * LPR) * 4;
+            float4 acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < N; ++j) {
+                const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
+                const float4 g0 = *reinterpret_cast<const float4*>(gm + j * NP + i0);
+                const float4 g1 = *reinterpret_cast<const float4*>(gm + j * NP + i0 + 4);
+                const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    acc[r].x = fmaf(gg[r], v.x, acc[r].x);
+                    acc[r].y = fmaf(gg[r], v.y, acc[r].y);
+                    acc[r].z = fmaf(gg[r], v.z, acc[r].z);
+                    acc[r].w = fmaf(gg[r], v.w, acc[r].w);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int i = i0 + r;
+                if (i >= N) break;
+                if (i == 0) {
+                    float4 u;
+                    u.x = go[col] + acc[0].x;
+                    u.y = go[col + 1] + acc[0].y;
+                    u.z = go[col + 2] + acc[0].z;
+                    u.w = go[col + 3] + acc[0].w;
+                    *reinterpret_cast<float4*>(a.grad_dense + b * D + col) = u;
+                } else {
+                    *reinterpret_cast<float4*>(dP + (b * T + (i - 1)) * D + col) = acc[r];
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 2. Lookup keys: key = global row id (row_base[t] + index), value = the dP
+// row of the lookup's bag (b*T + t).  Lookups that update nothing keep the
+// sentinel key (written first by a fill), which sorts last.
+// ---------------------------------------------------------------------------
+__global__ void fill_u32_kernel(uint32_t* p, int64_t n, uint32_t v)
+{
+    for (int64_t i = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; i < n; i += int64_t{gridDim.x} * blockDim.x)
+        p[i] = v;
+}
+
+template <typename TI>
+__global__ void expand_keys_kernel(const __grid_constant__ BwdArgs a, uint32_t* __restrict__ keys,
+                                   uint32_t* __restrict__ vals)
+{
+    const int64_t nbags = static_cast<int64_t>(a.T) * a.B;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (ld_index<TI>(a.offsets, 0) != 0 || ld_index<TI>(a.offsets, nbags) != a.nnz)
+            flag_status(a.status, DLRM_ERR_BAD_OFFSETS);
+    }
+    for (int64_t bag = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; bag < nbags;
+         bag += int64_t{gridDim.x} * blockDim.x) {
+        const int t = static_cast<int>(bag / a.B);
+        const int64_t b = bag - int64_t{t} * a.B;
+        const int64_t s0 = ld_index<TI>(a.offsets, bag), s1 = ld_index<TI>(a.offsets, bag + 1);
+        if (s0 < 0 || s1 < s0 || s1 > a.nnz) {
+            flag_status(a.status, DLRM_ERR_BAD_OFFSETS);
+            continue;
+        }
+        const uint32_t v = static_cast<uint32_t>(b * a.T + t);
+        for (int64_t p = s0; p < s1; ++p) {
+            const int64_t r = ld_index<TI>(a.indices, p);
+            if (r < 0 || r >= a.num_rows[t]) {
+                flag_status(a.status, DLRM_ERR_INDEX_OOB);
+                continue;
+            }
+            keys[p] = static_cast<uint32_t>(a.row_base[t] + r);
+            vals[p] = v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 3. Stable LSD radix sort of (key, value) pairs by key, 8 bits per pass.
+//    hist:    digit counts per tile of 4096 pairs   -> counts[digit][tile]
+//    scan:    per digit, exclusive scan over tiles; digit totals
+//    scatter: each pair to digit base + tile offset + its stable rank among
+//             equal digits of the tile (earlier positions first)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(const uint32_t* __restrict__ keys, int64_t n,
+                                                                  int shift, uint32_t* __restrict__ counts,
+                                                                  int64_t num_tiles)
+{
+    __shared__ uint32_t h[kBins];
+    for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+    __syncthreads();
+    const int64_t tile = blockIdx.x;
+    const int64_t t0 = tile * kSortTile;
+#pragma unroll 4
+    for (int i = 0; i < kSortItems; ++i) {
+        const int64_t p = t0 + i * kSortThreads + threadIdx.x;
+        if (p < n) atomicAdd(&h[(keys[p] >> shift) & (kBins - 1)], 1u);
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < kBins; d += blockDim.x) counts[d * num_tiles + tile] = h[d];
+}
+
+// One CTA per digit: in-place exclusive scan of counts[digit][0..num_tiles).
+__global__ void __launch_bounds__(256) radix_scan_kernel(uint32_t* __restrict__ counts, int64_t num_tiles,
+                                                         uint32_t* __restrict__ bin_total)
+{
+    __shared__ uint32_t warp_sum[8];
+    __shared__ uint32_t carry;
+    uint32_t* row = counts + blockIdx.x * num_tiles;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t base = 0; base < num_tiles; base += 256) {
+        const int64_t i = base + threadIdx.x;
+        const uint32_t v = i < num_tiles ? row[i] : 0u;
+        uint32_t x = v;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, s);
+            if (lane >= s) x += y;
+        }
+        if (lane == 31) warp_sum[warp] = x;
+        __syncthreads();
+        uint32_t before = carry;
+        for (int w = 0; w < warp; ++w) before += warp_sum[w];
+        if (i < num_tiles) row[i] = before + x - v;
+        __syncthreads();
+        if (threadIdx.x == 255) carry = before + x;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) bin_total[blockIdx.x] = carry;
+}
+
+__global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
+    const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
+    uint32_t* __restrict__ vals_out, int64_t n, int shift, const uint32_t* __restrict__ counts, int64_t num_tiles,
+    const uint32_t* __restrict__ bin_total)
+{
+    constexpr int kWarps = kSortThreads / kWarp;
+    constexpr int kPerWarp = kSortTile / kWarps;  // 512 consecutive pairs per warp
+    __shared__ uint32_t warp_cnt[kWarps][kBins];
+    __shared__ uint32_t base_of[kBins];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t tile = blockIdx.x;
+
+    for (int i = threadIdx.x; i < kWarps * kBins; i += blockDim.x) (&warp_cnt[0][0])[i] = 0;
+    // digit bases: exclusive scan of the digit totals (kBins values, one thread each)
+    {
+        const int d = threadIdx.x;  // kSortThreads == kBins
+        const uint32_t v = bin_total[d];
+        uint32_t x = v;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, s);
+            if (lane >= s) x += y;
+        }
+        __shared__ uint32_t wsum[kWarps];
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        uint32_t before = 0;
+        for (int w = 0; w < warp; ++w) before += wsum[w];
+        base_of[d] = before + x - v + counts[d * num_tiles + tile];
+    }
+    __syncthreads();
+
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    const int64_t w0 = tile * kSortTile + warp * kPerWarp;
+    uint32_t key[kPerWarp / kWarp], val[kPerWarp / kWarp], rank[kPerWarp / kWarp];
+#pragma unroll
+    for (int r = 0; r < kPerWarp / kWarp; ++r) {
+        const int64_t p = w0 + r * kWarp + lane;
+        const bool live = p < n;
+        key[r] = live ? keys_in[p] : 0u;
+        val[r] = live ? vals_in[p] : 0u;
+        const uint32_t d = (key[r] >> shift) & (kBins - 1);
+        const uint32_t live_mask = __ballot_sync(0xffffffffu, live);
+        uint32_t peers = __match_any_sync(0xffffffffu, live ? d : 0xFFFFFFFFu) & live_mask;
+        const uint32_t before = warp_cnt[warp][d];
+        rank[r] = before + __popc(peers & lt_mask);
+        __syncwarp();
+        if (live && (peers & ~((lt_mask << 1) | 1u)) == 0) warp_cnt[warp][d] = before + __popc(peers);  // last peer
+        __syncwarp();
+    }
+    __syncthreads();
+    // exclusive prefix of the per-warp digit counts across warps (warp order = position order)
+    {
+        const int d = threadIdx.x;
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t c = warp_cnt[w][d];
+            warp_cnt[w][d] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kPerWarp / kWarp; ++r) {
+        const int64_t p = w0 + r * kWarp + lane;
+        if (p < n) {
+            const uint32_t d = (key[r] >> shift) & (kBins - 1);
+            const uint32_t dst = base_of[d] + warp_cnt[warp][d] + rank[r];
+            keys_out[dst] = key[r];
+            vals_out[dst] = val[r];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 4. Ordered per-row gradient sums and row-wise Adagrad.
+// Sorted lookups are cut into chunks of kChunk.  One warp per chunk walks its
+// lookups in order and sums dP rows run by run (a run = equal keys).  A run
+// that lies inside its chunk is finished at once (Adagrad on its row).  A run
+// cut by a chunk border leaves a partial sum: the chunk's first run in slot
+// 2c, its last run (if different) in slot 2c+1; a second kernel adds the
+// pieces of each cut run in chunk order and applies Adagrad.
+// ---------------------------------------------------------------------------
+// lane owns elements [4*lane, 4*lane+4) (+128 for D = 256) when D >= 128;
+// for D < 128 lanes 0..D/4-1 own one float4 each.
+template <int D>
+struct Lanes {
+    static constexpr int kChunks = D >= 128 ? D / 128 : 1;
+    static constexpr int kActive = D >= 128 ? kWarp : D / 4;
+};
+
+template <int D>
+__device__ __forceinline__ void adagrad_row(const BwdArgs& a, uint32_t key, int t, const float4 (&g)[Lanes<D>::kChunks],
+                                            int lane)
+{
+    constexpr int C = Lanes<D>::kChunks;
+    const bool active = lane < Lanes<D>::kActive;
+    float ss = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < C; ++k) ss += g[k].x * g[k].x + g[k].y * g[k].y + g[k].z * g[k].z + g[k].w * g[k].w;
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
+    const int64_t r = static_cast<int64_t>(key) - a.row_base[t];
+    float* acc = a.accum[t] + r;
+    const float A = *acc + ss / static_cast<float>(D);
+    const float den = sqrtf(A) + a.eps;
+    if (active) {
+        float* w = a.tables[t] + r * D;
+#pragma unroll
+        for (int k = 0; k < C; ++k) {
+            const int col = (lane + k * kWarp) * 4;
+            float4 v = *reinterpret_cast<float4*>(w + col);
+            v.x -= a.lr * g[k].x / den;
+            v.y -= a.lr * g[k].y / den;
+            v.z -= a.lr * g[k].z / den;
+            v.w -= a.lr * g[k].w / den;
+            *reinterpret_cast<float4*>(w + col) = v;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) *acc = A;
+}
+
+template <int D, typename TI>
+__global__ void __launch_bounds__(256) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
+                                                            const uint32_t* __restrict__ keys,
+                                                            const uint32_t* __restrict__ vals,
+                                                            const float* __restrict__ dP,
+                                                            float* __restrict__ partial, int64_t num_chunks)
+{
+    constexpr int C = Lanes<D>::kChunks;
+    constexpr int U = 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t chunk = blockIdx.x * int64_t{blockDim.x / kWarp} + (threadIdx.x >> 5);
+    if (chunk >= num_chunks) return;
+    const bool active = lane < Lanes<D>::kActive;
+    const int64_t c0 = chunk * kChunk;
+    const int64_t c1 = min(c0 + kChunk, a.nnz);
+    const uint32_t before_key = c0 > 0 ? keys[c0 - 1] : kSentinel;
+    const uint32_t after_key = c1 < a.nnz ? keys[c1] : kSentinel;
+
+    uint32_t cur = kSentinel;
+    int cur_t = 0;
+    bool cur_first = true;  // current run is the chunk's first run
+    float4 g[C];
+#pragma unroll
+    for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    auto flush = [&]() {
+        if (cur == kSentinel) return;
+        const bool cut_before = cur_first && before_key == cur;
+        const bool cut_after = after_key == cur;
+        if (!cut_before && !cut_after) {
+            adagrad_row<D>(a, cur, cur_t, g, lane);
+        } else {
+            float* dst = partial + ((chunk * 2) + (cur_first ? 0 : 1)) * D;
+            if (active) {
+#pragma unroll
+                for (int k = 0; k < C; ++k) *reinterpret_cast<float4*>(dst + (lane + k * kWarp) * 4) = g[k];
+            }
+        }
+    };
+
+    for (int64_t base = c0; base < c1; base += kWarp) {
+        const int64_t p = base + lane;
+        const uint32_t kk = p < c1 ? keys[p] : kSentinel;
+        const uint32_t vv = p < c1 ? vals[p] : 0u;
+        const int nq = static_cast<int>(c1 - base < kWarp ? c1 - base : kWarp);
+        for (int j0 = 0; j0 < nq; j0 += U) {
+            float4 row[U][C];
+            uint32_t kj[U];
+            float sc[U];
+            int tj[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = j0 + u;
+                kj[u] = __shfl_sync(0xffffffffu, kk, j & 31);
+                const uint32_t vj = __shfl_sync(0xffffffffu, vv, j & 31);
+                const bool live = j < nq && kj[u] != kSentinel;
+                if (!live) kj[u] = kSentinel;
+                tj[u] = static_cast<int>(vj % static_cast<uint32_t>(a.T));
+                sc[u] = 1.0f;
+                if (live && a.mean) {
+                    const int64_t b = vj / static_cast<uint32_t>(a.T);
+                    const int64_t bag = static_cast<int64_t>(tj[u]) * a.B + b;
+                    const int64_t L = ld_index<TI>(a.offsets, bag + 1) - ld_index<TI>(a.offsets, bag);
+                    sc[u] = 1.0f / static_cast<float>(L);
+                }
+                if (live && active) {
+                    const float* src = dP + static_cast<int64_t>(vj) * D;
+#pragma unroll
+                    for (int k = 0; k < C; ++k) row[u][k] = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (kj[u] == kSentinel) continue;
+                if (kj[u] != cur) {
+                    flush();
+                    cur_first = (cur == kSentinel);
+                    cur = kj[u];
+                    cur_t = tj[u];
+#pragma unroll
+                    for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (active) {
+#pragma unroll
+                    for (int k = 0; k < C; ++k) {
+                        g[k].x = fmaf(row[u][k].x, sc[u], g[k].x);
+                        g[k].y = fmaf(row[u][k].y, sc[u], g[k].y);
+                        g[k].z = fmaf(row[u][k].z, sc[u], g[k].z);
+                        g[k].w = fmaf(row[u][k].w, sc[u], g[k].w);
+                    }
+                }
+            }
+        }
+    }
+    flush();
+}
+
+// One warp per chunk that holds the start of a run cut by its end border.
+template <int D>
+__global__ void __launch_bounds__(256) segment_span_kernel(const __grid_constant__ BwdArgs a,
+                                                           const uint32_t* __restrict__ keys,
+                                                           const uint32_t* __restrict__ vals,
+                                                           const float* __restrict__ partial, int64_t num_chunks)
+{
+    constexpr int C = Lanes<D>::kChunks;
+    const int lane = threadIdx.x & 31;
+    const int64_t chunk = blockIdx.x * int64_t{blockDim.x / kWarp} + (threadIdx.x >> 5);
+    if (chunk >= num_chunks) return;
+    const bool active = lane < Lanes<D>::kActive;
+    const int64_t c0 = chunk * kChunk;
+    const int64_t c1 = min(c0 + kChunk, a.nnz);
+    if (c1 >= a.nnz) return;  // last chunk: nothing runs past it
+    const uint32_t key = keys[c1 - 1];
+    if (key == kSentinel || keys[c1] != key) return;     // last run not cut
+    const bool whole = keys[c0] == key;                   // chunk is one run
+    if (whole && c0 > 0 && keys[c0 - 1] == key) return;   // run started in an earlier chunk
+    const int t = static_cast<int>(vals[c1 - 1] % static_cast<uint32_t>(a.T));
+
+    float4 g[C];
+#pragma unroll
+    for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](int64_t slot) {
+        if (!active) return;
+        const float* src = partial + slot * D;
+#pragma unroll
+        for (int k = 0; k < C; ++k) {
+            const float4 v = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
+            g[k].x += v.x;
+            g[k].y += v.y;
+            g[k].z += v.z;
+            g[k].w += v.w;
+        }
+    };
+    add(chunk * 2 + (whole ? 0 : 1));
+    for (int64_t c = chunk + 1; c < num_chunks; ++c) {
+        add(c * 2);
+        const int64_t e = min((c + 1) * kChunk, a.nnz);
+        if (e >= a.nnz || keys[e] != key) break;
+    }
+    adagrad_row<D>(a, key, t, g, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+constexpr int kMaxSmem = 227 * 1024;
+
+template <int D, int G>
+dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
+{
+    const BwdLayout l = make_bwd_layout(a.T, D);
+    int groups = 1;
+    if (G == 1) {
+        groups = kMaxSmem / l.bytes;
+        if (groups > 4) groups = 4;
+        if (groups < 1) return DLRM_ERR_UNSUPPORTED;
+    } else if (l.bytes > kMaxSmem) {
+        return DLRM_ERR_UNSUPPORTED;
+    }
+    const size_t smem = static_cast<size_t>(groups) * l.bytes;
+    auto kern = interact_bwd_kernel<D, G>;
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    const int64_t blocks = (a.B + groups - 1) / groups;
+    kern<<<static_cast<unsigned>(blocks), groups * G * kWarp, smem, s>>>(a, dP, groups);
+    return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
+}
+
+template <int D, typename TI>
+dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
+{
+    // interaction backward: a sample's g V is shared by 8 warps for wide N
+    const int nblk = round_up(a.T + 1, 8) / 8;
+    dlrm_status st = nblk > 8 ? launch_interact_bwd<D, 8>(a, w.dP, s) : launch_interact_bwd<D, 1>(a, w.dP, s);
+    if (st != DLRM_OK) return st;
+    if (a.nnz == 0) return DLRM_OK;
+
+    const int64_t nbags = int64_t{a.T} * a.B;
+    fill_u32_kernel<<<148 * 8, 256, 0, s>>>(w.keys[0], a.nnz, kSentinel);
+    expand_keys_kernel<TI><<<static_cast<unsigned>((nbags + 255) / 256 < 148 * 64 ? (nbags + 255) / 256 : 148 * 64), 256, 0, s>>>(
+        a, w.keys[0], w.vals[0]);
+
+    // key bits: valid keys are < total rows, so the sentinel's low bits sort after them
+    int bits = 1;
+    while ((int64_t{1} << bits) <= a.row_base[a.T]) ++bits;
+    int cur = 0;
+    for (int shift = 0; shift < bits; shift += kRadixBits) {
+        radix_hist_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, 0, s>>>(w.keys[cur], a.nnz, shift,
+                                                                                     w.counts, w.num_tiles);
+        radix_scan_kernel<<<kBins, 256, 0, s>>>(w.counts, w.num_tiles, w.bin_total);
+        radix_scatter_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, 0, s>>>(
+            w.keys[cur], w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], a.nnz, shift, w.counts, w.num_tiles,
+            w.bin_total);
+        cur ^= 1;
+    }
+    const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + 7) / 8);
+    segment_chunk_kernel<D, TI><<<seg_blocks, 256, 0, s>>>(a, w.keys[cur], w.vals[cur], w.dP, w.partial,
+                                                           w.num_chunks);
+    segment_span_kernel<D><<<seg_blocks, 256, 0, s>>>(a, w.keys[cur], w.vals[cur], w.partial, w.num_chunks);
+    return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
+}
+
+template <int D>
+dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, cudaStream_t s)
+{
+    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, s) : run_backward<D, int64_t>(a, w, s);
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz)
+{
+    size_t total = 0;
+    carve(nullptr, B, T, D, nnz, &total);
+    return total;
+}
+
+dlrm_status launch_backward(const BwdArgs& a, int dim, int index_type, void* workspace, size_t workspace_bytes,
+                            cudaStream_t s)
+{
+    size_t need = 0;
+    const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, &need);
+    if (workspace_bytes < need) return DLRM_ERR_INVALID_ARG;
+    switch (dim) {
+        case 16: return dispatch_bwd<16>(a, index_type, w, s);
+        case 32: return dispatch_bwd<32>(a, index_type, w, s);
+        case 64: return dispatch_bwd<64>(a, index_type, w, s);
+        case 128: return dispatch_bwd<128>(a, index_type, w, s);
+        case 256: return dispatch_bwd<256>(a, index_type, w, s);
+        default: return DLRM_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace dlrm

@@ -1,0 +1,67 @@
+// internal.h -- launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+#include "dlrm_sparse.h"
+
+namespace dlrm {
+
+enum FwdMode : int {
+    kEmbbag = 0,    // gather + pool, write pooled
+    kFused = 1,     // gather + pool + interaction, write out (and pooled if asked)
+    kInteract = 2,  // interaction of given dense + pooled, write out
+};
+
+// Everything a forward kernel needs, passed by value as one kernel parameter.
+struct FwdArgs {
+    const void* tables[DLRM_MAX_TABLES];
+    int64_t num_rows[DLRM_MAX_TABLES];
+    const void* indices;
+    const void* offsets;
+    const float* dense;
+    const float* pooled_in;
+    float* out;
+    float* pooled_out;
+    int32_t* status;
+    int64_t B;
+    int64_t nnz;
+    int32_t T;
+    int32_t mean;
+};
+
+// Launch one forward pass.  dim in {16,32,64,128,256}; dtype/index_type as in
+// the ABI.  Returns DLRM_OK, DLRM_ERR_UNSUPPORTED or DLRM_ERR_CUDA.
+dlrm_status launch_forward(int mode, const FwdArgs& args, int dim, int dtype, int index_type,
+                           cudaStream_t stream);
+
+// ---- training step -------------------------------------------------------
+struct BwdArgs {
+    float* tables[DLRM_MAX_TABLES];
+    float* accum[DLRM_MAX_TABLES];
+    int64_t num_rows[DLRM_MAX_TABLES];
+    int64_t row_base[DLRM_MAX_TABLES + 1];  // prefix sum of num_rows
+    const void* indices;
+    const void* offsets;
+    const float* dense;
+    const float* pooled;
+    const float* grad_out;
+    float* grad_dense;
+    int32_t* status;
+    int64_t B;
+    int64_t nnz;
+    int32_t T;
+    int32_t mean;
+    float lr;
+    float eps;
+};
+
+size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz);
+
+dlrm_status launch_backward(const BwdArgs& args, int dim, int index_type, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+}  // namespace dlrm

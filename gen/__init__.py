@@ -135,18 +135,35 @@ def fill_table_device(ptr: int, dtype: str, seed: int, t: int, row0: int, nrows:
 # --------------------------------------------------------------------------
 # Index distributions.
 # --------------------------------------------------------------------------
-def zipf_cdf(V: int, alpha: float) -> np.ndarray:
-    """Unnormalised CDF of p(k) ~ k^-alpha on k = 1..V (float64)."""
-    k = np.arange(1, V + 1, dtype=np.float64)
-    np.power(k, -alpha, out=k)
-    return np.cumsum(k, out=k)
+def zipf_ranks(rng: np.random.Generator, V: int, alpha: float, n: int) -> np.ndarray:
+    """n exact draws of k in 1..V with p(k) ~ k^-alpha (alpha > 0, alpha != 1).
 
+    Rejection from a continuous envelope: x^-alpha is convex, so its integral
+    over [k-1/2, k+1/2] is at least k^-alpha (Hermite-Hadamard).  Draw X with
+    density ~ x^-alpha on [1/2, V+1/2] by inverting its antiderivative
+    H(x) = x^(1-alpha) / (1-alpha), round to k, and keep k with probability
+    k^-alpha / (H(k+1/2) - H(k-1/2)).  (The envelope is the one of Hoermann &
+    Derflinger's rejection-inversion, 1996; here with a second uniform.)"""
+    a1 = 1.0 - alpha
 
-def zipf_ranks(rng: np.random.Generator, cdf: np.ndarray, n: int) -> np.ndarray:
-    """n ranks in 1..V drawn by inverting the exact CDF."""
-    u = rng.random(n) * cdf[-1]
-    k = np.searchsorted(cdf, u, side="right") + 1
-    return np.minimum(k, cdf.size).astype(np.int64)
+    def H(x):
+        return np.power(x, a1) / a1
+
+    def H_inv(y):
+        return np.power(y * a1, 1.0 / a1)
+
+    lo, hi = H(0.5), H(V + 0.5)
+    out = np.empty(n, dtype=np.int64)
+    filled = 0
+    while filled < n:
+        m = int((n - filled) * 1.15) + 16
+        x = H_inv(lo + rng.random(m) * (hi - lo))
+        k = np.clip(np.floor(x + 0.5), 1, V)
+        keep = rng.random(m) * (H(k + 0.5) - H(k - 0.5)) <= np.power(k, -alpha)
+        got = k[keep].astype(np.int64)[: n - filled]
+        out[filled:filled + got.size] = got
+        filled += got.size
+    return out
 
 
 def affine_perm_params(seed: int, t: int, V: int) -> tuple[int, int]:
@@ -273,15 +290,9 @@ def make_batches(w: Workload, batch_ids, with_grad: bool | None = None) -> list:
     rngs = {b: np.random.default_rng([w.seed, 1, b]) for b in batch_ids}
     lengths = {b: [] for b in batch_ids}
     idx = {b: [] for b in batch_ids}
-    cdf_cache = {}
     for t in range(w.T):
         V = int(w.num_rows[t])
         if w.index_dist == "zipf":
-            key = (V, w.alpha)
-            if key not in cdf_cache:
-                cdf_cache.clear()
-                cdf_cache[key] = zipf_cdf(V, w.alpha)
-            cdf = cdf_cache[key]
             a, c = affine_perm_params(w.seed, t, V)
         for b in batch_ids:
             rng = rngs[b]
@@ -291,7 +302,7 @@ def make_batches(w: Workload, batch_ids, with_grad: bool | None = None) -> list:
                 L = rng.integers(w.bag_min, w.bag_max + 1, size=w.B)
             n = int(L.sum())
             if w.index_dist == "zipf":
-                rows = permute(zipf_ranks(rng, cdf, n) - 1, a, c, V)
+                rows = permute(zipf_ranks(rng, V, w.alpha, n) - 1, a, c, V)
             else:
                 rows = rng.integers(0, V, size=n)
             lengths[b].append(L)

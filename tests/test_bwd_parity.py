@@ -1,0 +1,186 @@
+"""GPU parity of dlrm_sparse_bwd_adagrad (through the C ABI) with the CPU oracle:
+grad_dense, every touched row and accumulator, untouched rows bit-identical,
+bitwise reproducibility, long runs of one row crossing many reduction chunks."""
+import numpy as np
+import pytest
+import torch
+
+import embedding_bag_lookup_dlrm_b300 as dl
+import gen
+import oracle
+from gpu_util import (TOL_ADAGRAD, TOL_INTERACT, assert_close, batch_to_device, dev_index, dev_tables, free_cuda,
+                      random_case, workload_tables)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def run_case(orc, tabs, Vs, idx, off, dense, mode, itype, lr=0.01, eps=1e-8, acc0=0.1, seed=0):
+    B, D = dense.shape
+    T = len(tabs)
+    N = T + 1
+    rng = np.random.default_rng(seed + 1)
+    g = rng.standard_normal((B, D + N * (N - 1) // 2)).astype(np.float32)
+    pooled, st = orc.embbag(tabs, Vs, idx, off, B, D, mode)
+    new_ref = [t.copy() for t in tabs]
+    acc_ref = [np.full(v, acc0, np.float32) for v in Vs]
+    gd_ref, st2 = orc.sparse_bwd_adagrad(new_ref, Vs, idx, off, dense, pooled, g, acc_ref, lr, eps, mode)
+
+    dt = dev_tables(tabs, "f32")
+    acc = [torch.full((v,), acc0, dtype=torch.float32, device="cuda") for v in Vs]
+    di, do = dev_index(idx, itype), dev_index(off, itype)
+    dx = torch.from_numpy(dense).cuda()
+    ps = torch.empty((B, T, D), dtype=torch.float32, device="cuda")
+    dl.dlrm_sparse_fwd(dt, di, do, dx, mode, pooled_save=ps)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gd = dl.dlrm_sparse_bwd_adagrad(dt, acc, di, do, dx, ps, torch.from_numpy(g).cuda(), lr, eps, mode,
+                                    status=status)
+    torch.cuda.synchronize()
+    return dict(g=g, pooled=pooled, new_ref=new_ref, acc_ref=acc_ref, gd_ref=gd_ref, st_ref=st | st2,
+                dt=dt, acc=acc, gd=gd.cpu().numpy(), status=status.item())
+
+
+def check(res, tabs, Vs, idx, off, B, dense):
+    assert res["status"] == res["st_ref"] == 0
+    T = len(tabs)
+    D = dense.shape[1]
+    g = res["g"]
+    # scale of grad_dense: |g_x| + sum_j |g_0j| |V_j|
+    Vabs = np.concatenate([np.abs(dense)[:, None], np.abs(res["pooled"])], axis=1)
+    s = np.abs(g[:, :D]) + np.einsum("bj,bjd->bd", np.abs(g[:, D:D + T]), Vabs[:, 1:])
+    assert_close(res["gd"], res["gd_ref"], s, TOL_INTERACT, "grad_dense")
+    for t in range(T):
+        got = res["dt"][t].cpu().numpy()
+        acc = res["acc"][t].cpu().numpy()
+        touched = np.zeros(Vs[t], bool)
+        seg = idx[off[t * B]:off[(t + 1) * B]]
+        touched[seg[(seg >= 0) & (seg < Vs[t])]] = True
+        # untouched rows and accumulators are bit-identical
+        assert np.array_equal(got[~touched], tabs[t][~touched])
+        assert np.all(acc[~touched] == res["acc_ref"][t][~touched])
+        # touched rows: the update is small against the weights, so measure it
+        # against |w| + |w - w_new| (the size of the step taken)
+        scale = np.abs(tabs[t][touched]) + np.abs(tabs[t][touched] - res["new_ref"][t][touched])
+        assert_close(got[touched], res["new_ref"][t][touched], scale, TOL_ADAGRAD, f"rows of table {t}")
+        assert_close(acc[touched], res["acc_ref"][t][touched], 0.0, TOL_ADAGRAD, f"accum of table {t}")
+        # the update itself, against the step size
+        step_ref = res["new_ref"][t][touched].astype(np.float64) - tabs[t][touched]
+        step = got[touched].astype(np.float64) - tabs[t][touched]
+        assert_close(step, step_ref, np.abs(step_ref).max() * 1e-3 + 1e-12, 1e-2, f"steps of table {t}")
+
+
+CASES = [
+    # D, T, mode, itype, Lmin, Lmax, B, V
+    (128, 26, "sum", "i32", 1, 8, 200, 300),
+    (128, 26, "mean", "i64", 0, 8, 97, 300),
+    (64, 5, "sum", "i32", 0, 30, 301, 40),
+    (16, 3, "mean", "i32", 1, 3, 1000, 7),
+    (256, 2, "sum", "i64", 1, 1, 33, 1000),
+    (32, 100, "sum", "i32", 1, 2, 21, 100),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "D{}-T{}-{}-{}-L{}..{}-B{}-V{}".format(*c))
+def test_bwd_adagrad_random(case, orc):
+    D, T, mode, itype, Lmin, Lmax, B, V = case
+    tabs, Vs, idx, off, dense = random_case(200 + CASES.index(case), B, T, D, V, Lmin, Lmax, value_scale=0.05)
+    res = run_case(orc, tabs, Vs, idx, off, dense, mode, itype, seed=CASES.index(case))
+    check(res, tabs, Vs, idx, off, B, dense)
+
+
+def test_long_runs_cross_chunks(orc):
+    """One row looked up ~5000 times (twenty reduction chunks), others rarely."""
+    B, T, D, V = 2500, 2, 128, 50
+    rng = np.random.default_rng(3)
+    tabs = [rng.uniform(-0.05, 0.05, size=(V, D)).astype(np.float32) for _ in range(T)]
+    L = np.full(T * B, 2)
+    off = np.concatenate([[0], np.cumsum(L)])
+    idx = rng.integers(0, V, size=int(L.sum()))
+    idx[: 2 * B] = np.where(rng.random(2 * B) < 0.97, 7, idx[: 2 * B])  # table 0: row 7 dominates
+    dense = rng.standard_normal((B, D)).astype(np.float32)
+    res = run_case(orc, tabs, [V] * T, idx, off, dense, "sum", "i32", lr=0.05)
+    check(res, tabs, [V] * T, idx, off, B, dense)
+
+
+def test_bwd_bitwise_reproducible():
+    B, T, D, V = 4000, 26, 128, 400
+    tabs, Vs, idx, off, dense = random_case(31, B, T, D, V, 1, 8, value_scale=0.05)
+    rng = np.random.default_rng(1)
+    g = torch.from_numpy(rng.standard_normal((B, D + 27 * 13)).astype(np.float32)).cuda()
+    di, do, dx = dev_index(idx, "i32"), dev_index(off, "i32"), torch.from_numpy(dense).cuda()
+    results = []
+    for _ in range(2):
+        dt = dev_tables(tabs, "f32")
+        acc = [torch.full((v,), 0.1, device="cuda") for v in Vs]
+        ps = torch.empty((B, T, D), device="cuda")
+        dl.dlrm_sparse_fwd(dt, di, do, dx, pooled_save=ps)
+        gd = dl.dlrm_sparse_bwd_adagrad(dt, acc, di, do, dx, ps, g, 0.01, 1e-8)
+        torch.cuda.synchronize()
+        results.append((torch.cat([t.flatten() for t in dt]), torch.cat(acc), gd))
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
+
+
+def test_bwd_flags_bad_index(orc):
+    B, T, D, V = 50, 3, 64, 30
+    tabs, Vs, idx, off, dense = random_case(41, B, T, D, V, 1, 3, value_scale=0.05)
+    idx[4] = V + 5
+    dt = dev_tables(tabs, "f32")
+    acc = [torch.full((v,), 0.1, device="cuda") for v in Vs]
+    ps = torch.empty((B, T, D), device="cuda")
+    di, do, dx = dev_index(idx, "i32"), dev_index(off, "i32"), torch.from_numpy(dense).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dl.dlrm_sparse_fwd(dt, di, do, dx, pooled_save=ps, status=status)
+    g = torch.randn((B, D + 6), device="cuda")
+    dl.dlrm_sparse_bwd_adagrad(dt, acc, di, do, dx, ps, g, 0.01, 1e-8, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & dl.DLRM_ERR_INDEX_OOB
+
+
+def test_workload_training_step(orc):
+    """The full training-step workload: B=32768, T=26 fp32 tables of 2e6 rows, bags 1..8, Zipf(1.05)."""
+    w = gen.workload(5)
+    batch, = gen.make_batches(w, [0])
+    tabs_host, nr, cidx = gen.compact_tables(w, batch)
+    pooled, st = orc.embbag(tabs_host, nr, cidx, batch.offsets, w.B, w.D, w.mode)
+    new_ref = [t.copy() for t in tabs_host]
+    acc_ref = [np.full(n, w.accum_init, np.float32) for n in nr]
+    gd_ref, st2 = orc.sparse_bwd_adagrad(new_ref, nr, cidx, batch.offsets, batch.dense, pooled, batch.grad_out,
+                                         acc_ref, w.lr, w.eps, w.mode)
+    assert st == 0 and st2 == 0
+
+    tabs = workload_tables(w)
+    acc = [torch.full((V,), w.accum_init, dtype=torch.float32, device="cuda") for V in w.num_rows]
+    di, do, dx = batch_to_device(batch)
+    ps = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dl.dlrm_sparse_fwd(tabs, di, do, dx, w.mode, pooled_save=ps, status=status)
+    gd = dl.dlrm_sparse_bwd_adagrad(tabs, acc, di, do, dx, ps, torch.from_numpy(batch.grad_out).cuda(), w.lr,
+                                    w.eps, w.mode, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    N = w.T + 1
+    Vabs = np.abs(pooled)
+    s = np.abs(batch.grad_out[:, :w.D]) + np.einsum("bj,bjd->bd", np.abs(batch.grad_out[:, w.D:w.D + w.T]), Vabs)
+    assert_close(gd.cpu().numpy(), gd_ref, s, TOL_INTERACT, "grad_dense")
+    off = batch.offsets.astype(np.int64)
+    for t in range(w.T):
+        rows = np.unique(batch.indices[off[t * w.B]:off[(t + 1) * w.B]]).astype(np.int64)
+        got = tabs[t][torch.from_numpy(rows).cuda()].cpu().numpy()
+        got_acc = acc[t][torch.from_numpy(rows).cuda()].cpu().numpy()
+        scale = np.abs(tabs_host[t]) + np.abs(tabs_host[t] - new_ref[t])
+        assert_close(got, new_ref[t], scale, TOL_ADAGRAD, f"rows of table {t}")
+        assert_close(got_acc, acc_ref[t], 0.0, TOL_ADAGRAD, f"accum of table {t}")
+        # a sample of untouched rows still holds the generator's values
+        rng = np.random.default_rng(t)
+        probe = rng.integers(0, w.num_rows[t], size=64)
+        probe = probe[~np.isin(probe, rows)]
+        assert np.array_equal(tabs[t][torch.from_numpy(probe).cuda()].cpu().numpy(),
+                              gen.table_rows(w.seed, t, probe, w.D))
+        assert torch.all(acc[t][torch.from_numpy(probe).cuda()] == w.accum_init)
+    del tabs, acc, ps
+    free_cuda()

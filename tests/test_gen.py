@@ -31,17 +31,25 @@ def test_streams_differ_per_table_and_seed():
     assert not np.array_equal(a, gen.table_rows(2, 0, [5], 32))
 
 
-def test_zipf_frequencies():
+@pytest.mark.parametrize("V,alpha", [(1000, 1.05), (7, 1.1), (5_000_000, 1.1)])
+def test_zipf_frequencies(V, alpha):
+    """Rank counts against the exact probabilities k^-alpha / sum_j j^-alpha."""
     rng = np.random.default_rng(0)
-    cdf = gen.zipf_cdf(1000, 1.05)
-    k = gen.zipf_ranks(rng, cdf, 400_000)
-    assert k.min() >= 1 and k.max() <= 1000
-    p = np.arange(1, 1001, dtype=np.float64) ** -1.05
-    p /= p.sum()
-    counts = np.bincount(k, minlength=1001)[1:]
-    for r in (1, 2, 3, 10, 100):
-        exp = p[r - 1] * k.size
-        assert abs(counts[r - 1] - exp) < 5 * np.sqrt(exp), (r, counts[r - 1], exp)
+    n = 400_000
+    k = gen.zipf_ranks(rng, V, alpha, n)
+    assert k.min() >= 1 and k.max() <= V
+    Z = np.sum(np.arange(1, V + 1, dtype=np.float64) ** -alpha)
+    counts = np.bincount(k, minlength=min(V, 200) + 1)
+    for r in [1, 2, 3, 5, 7, 10, 100]:
+        if r > V:
+            continue
+        exp = r ** -alpha / Z * n
+        assert abs(counts[r] - exp) < 5 * np.sqrt(exp) + 1, (r, counts[r], exp)
+    # tail mass beyond rank 100 (or none)
+    if V > 100:
+        exp_tail = (1 - np.sum(np.arange(1, 101, dtype=np.float64) ** -alpha) / Z) * n
+        got_tail = np.sum(k > 100)
+        assert abs(got_tail - exp_tail) < 5 * np.sqrt(exp_tail), (got_tail, exp_tail)
 
 
 def test_affine_permutation_is_bijection():
