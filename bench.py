@@ -20,7 +20,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -39,18 +38,35 @@ FLUSH_BYTES = 512 << 20  # > 4x the 126 MB L2
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--max-rows", type=int, default=0,
+                   help="cap every table at this many rows (a small case of the same kernel, for profiling)")
+    p.add_argument("--uniform", action="store_true",
+                   help="uniform instead of Zipf indices (every lookup a likely DRAM read)")
     return p.parse_args()
 
 
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the slowest rank sets a job's time).
+    Ranks hold no data-path collective; this host-side reduction is the only
+    exchange, over the gloo process group."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def algorithmic_bytes(w: gen.Workload, batch: gen.Batch) -> int:
@@ -94,52 +110,70 @@ def sources_digest() -> str:
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event (throttle) reasons, polled through NVML every
+    `period` seconds on a background thread while the timed region runs.
+    Reading only: nothing here changes a GPU setting."""
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, gpu_index: int, period: float = 0.002):
+        self.gpu, self.period = gpu_index, period
+        self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
 
     def __enter__(self):
+        import threading
+        self._stop = threading.Event()
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            import pynvml as nv
+            nv.nvmlInit()
+            self._nv = nv
+            self._h = nv.nvmlDeviceGetHandleByIndex(self.gpu)
+            self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(self._h, nv.NVML_CLOCK_SM))
+            self._poll()
+        except Exception as e:  # no NVML: report the absence instead of guessing
+            self.error = repr(e)
+            self._nv = None
+            return self
+        self._t = threading.Thread(target=self._loop, daemon=True)
+        self._t.start()
         return self
 
-    def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
+    def _poll(self):
+        nv = self._nv
+        self.samples.append(float(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)))
+        mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+        for name, const in self.REASONS:
+            if mask & getattr(nv, const, 0):
+                self.reasons.add(name)
+
+    def _loop(self):
+        while not self._stop.is_set():
             try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self._poll()
+            except Exception as e:
+                self.error = repr(e)
+                return
+            time.sleep(self.period)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._nv is not None:
+            self._t.join(timeout=5)
+            try:
+                self._poll()
+                self._nv.nvmlShutdown()
+            except Exception:
+                pass
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        d = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+             "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "NVML, 2 ms polling"}
+        if self.error:
+            d["error"] = self.error
+        return d
 
 
 # ---------------------------------------------------------------------------
@@ -278,10 +312,7 @@ def run_ours(args, w):
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     value = w.B * world * args.steps / (total_ms / 1e3)
 
@@ -349,10 +380,7 @@ def run_e2e(args, w, tables, batches, dev, dl, torch, world):
         step(args.warmup + i)
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([el], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el = float(tt.item())
+    el = max_over_ranks(el, world)
     b0 = batches[0]
     h2d = int(np.mean([b.indices.nbytes + b.offsets.nbytes + b.dense.nbytes for b in batches]))
     d2h = w.B * w.out_width * 4
@@ -367,6 +395,12 @@ def main():
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     w = gen.workload(args.workload)
+    if args.max_rows > 0:
+        w.num_rows = [min(v, args.max_rows) for v in w.num_rows]
+        w.name += f" [tables capped at {args.max_rows} rows]"
+    if args.uniform:
+        w.index_dist = "uniform"
+        w.name += " [uniform indices]"
     if args.impl == "reference":
         run_reference(args, w)
     else:
