@@ -26,14 +26,15 @@ DLRM_ERR_TIMEOUT = 8
 DLRM_ERR_CUDA = 16
 DLRM_ERR_UNSUPPORTED = 32
 MAX_TABLES = 128
+STATIC_SCRATCH_BYTES = 32 << 20  # DLRM_STATIC_SCRATCH_BYTES
 
 _MODES = {"sum": 0, "mean": 1}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 _ITYPES = {torch.int32: 0, torch.int64: 1}
 
 C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sparse_fwd_host",
-             "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_status_string",
-             "dlrm_abi_version")
+             "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_adagrad_static",
+             "dlrm_status_string", "dlrm_abi_version")
 
 
 class DlrmTables(ctypes.Structure):
@@ -74,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dlrm_sparse_bwd_workspace_size": ([T, B, ctypes.POINTER(ctypes.c_size_t)], i32),
         "dlrm_sparse_bwd_adagrad": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p), ctypes.c_float,
                                      ctypes.c_float, P, ctypes.c_size_t, P, P], i32),
+        "dlrm_sparse_bwd_adagrad_static": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p),
+                                            ctypes.c_float, ctypes.c_float, P, P], i32),
         "dlrm_status_string": ([i32], ctypes.c_char_p),
         "dlrm_abi_version": ([], i32),
     }
@@ -283,4 +286,40 @@ def dlrm_sparse_bwd_adagrad(tables, accum, indices, offsets, dense, pooled_saved
                                      float(lr), float(eps), workspace.data_ptr(), workspace.numel(),
                                      status.data_ptr() if status is not None else None, _stream_ptr(stream))
     _raise(st, "dlrm_sparse_bwd_adagrad")
+    return grad_dense
+
+
+def dlrm_sparse_bwd_adagrad_static(tables, accum, indices, offsets, dense, pooled_saved, grad_out, lr, eps,
+                                   mode="sum", grad_dense=None, status=None, stream=None):
+    """dlrm_sparse_bwd_adagrad without a workspace: the C library uses its own
+    fixed scratch of STATIC_SCRATCH_BYTES per device, for callers that cannot
+    allocate device memory.  Pass grad_dense to keep this call free of
+    allocations on the Python side too.  Calls that overlap on the GPU share
+    the scratch and race.  Raises ValueError when the batch needs more
+    scratch than the fixed array holds."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    if len(accum) != tb.T:
+        raise ValueError("one accumulator per table")
+    for i, a in enumerate(accum):
+        _check_cuda(a, f"accum[{i}]", torch.float32)
+        if a.numel() != tb.tensors[i].shape[0]:
+            raise ValueError(f"accum[{i}] must hold one value per row")
+    for name, t in (("dense", dense), ("pooled_saved", pooled_saved), ("grad_out", grad_out)):
+        _check_cuda(t, name, torch.float32)
+    need = dlrm_sparse_bwd_workspace_size(tb, indices, offsets)
+    if need > STATIC_SCRATCH_BYTES:
+        raise ValueError(f"batch needs {need} bytes of scratch; the fixed scratch holds {STATIC_SCRATCH_BYTES}")
+    if grad_dense is None:
+        grad_dense = torch.empty((B, tb.D), dtype=torch.float32, device=dense.device)
+    _check_cuda(grad_dense, "grad_dense", torch.float32)
+    acc_ptrs = (ctypes.c_void_p * tb.T)(*[a.data_ptr() for a in accum])
+    bags = _bags(indices, offsets, B)
+    st = lib.dlrm_sparse_bwd_adagrad_static(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode],
+                                            dense.data_ptr(), pooled_saved.data_ptr(), grad_out.data_ptr(),
+                                            grad_dense.data_ptr(), acc_ptrs, float(lr), float(eps),
+                                            status.data_ptr() if status is not None else None,
+                                            _stream_ptr(stream))
+    _raise(st, "dlrm_sparse_bwd_adagrad_static")
     return grad_dense

@@ -169,6 +169,37 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables *tables, const dlrm_bags *
                                     void *workspace, size_t workspace_bytes,
                                     int32_t *status_dev, cudaStream_t stream);
 
+/* Bytes of the fixed scratch behind dlrm_sparse_bwd_adagrad_static. */
+#define DLRM_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* dlrm_sparse_bwd_adagrad for callers that cannot allocate device memory
+ * (the pages have no counterpart: this is a library convenience).  Such
+ * callers are, for example, a plugin reached through a plain C interface
+ * that receives only its input and output buffers, or a process whose device
+ * memory is owned by another framework's pooled allocator.  Instead of a
+ * caller workspace the step uses one fixed array of
+ * DLRM_STATIC_SCRATCH_BYTES of device memory that the library holds on every
+ * device that loads it, until the process exits.  Arguments, layouts and
+ * results are those of dlrm_sparse_bwd_adagrad without workspace /
+ * workspace_bytes.
+ *   - Returns DLRM_ERR_INVALID_ARG, before touching the GPU, when the batch
+ *     needs more scratch than DLRM_STATIC_SCRATCH_BYTES
+ *     (dlrm_sparse_bwd_workspace_size() says how much it needs).
+ *   - The first call on a device looks up the array's device address (and
+ *     so loads that part of the library onto the device); make that first
+ *     call before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU
+ *     (other streams, or host threads without ordering) race and must be
+ *     serialised by the caller.  No scratch contents carry over between
+ *     calls; nothing needs clearing.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree. */
+dlrm_status dlrm_sparse_bwd_adagrad_static(const dlrm_tables *tables, const dlrm_bags *bags,
+                                           dlrm_pool_mode mode, const float *dense,
+                                           const float *pooled_saved,
+                                           const float *grad_out, float *grad_dense,
+                                           float *const *accum, float lr, float eps,
+                                           int32_t *status_dev, cudaStream_t stream);
+
 /* A static, human-readable name of the lowest set status bit. */
 const char *dlrm_status_string(dlrm_status status);
 
