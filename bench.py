@@ -109,29 +109,70 @@ def sources_digest() -> str:
     return h.hexdigest()
 
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes)."""
+    CLOCK_SM = 1
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4), ("hw_power_brake", 0x80))
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+        except Exception:
+            pass
+        rc = -1
+        if uuid:
+            rc = self.lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError(f"no NVML handle ({rc})")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_mhz(self) -> float:
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v))
+        return float(v.value)
+
+    def max_sm_mhz(self) -> float:
+        v = self.ct.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v))
+        return float(v.value)
+
+    def reasons(self) -> int:
+        v = self.ct.c_ulonglong()
+        self._reasons_fn(self.h, self.ct.byref(v))
+        return int(v.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons, polled through NVML every
     `period` seconds on a background thread while the timed region runs.
     Reading only: nothing here changes a GPU setting."""
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
-               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
     def __init__(self, gpu_index: int, period: float = 0.002):
         self.gpu, self.period = gpu_index, period
         self.samples, self.reasons, self.max_mhz, self.error = [], set(), None, None
+        self._nv = None
 
     def __enter__(self):
         import threading
         self._stop = threading.Event()
         try:
-            import pynvml as nv
-            nv.nvmlInit()
-            self._nv = nv
-            self._h = nv.nvmlDeviceGetHandleByIndex(self.gpu)
-            self.max_mhz = float(nv.nvmlDeviceGetMaxClockInfo(self._h, nv.NVML_CLOCK_SM))
+            self._nv = _Nvml(self.gpu)
+            self.max_mhz = self._nv.max_sm_mhz()
             self._poll()
         except Exception as e:  # no NVML: report the absence instead of guessing
             self.error = repr(e)
@@ -142,11 +183,10 @@ class ClockSampler:
         return self
 
     def _poll(self):
-        nv = self._nv
-        self.samples.append(float(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)))
-        mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-        for name, const in self.REASONS:
-            if mask & getattr(nv, const, 0):
+        self.samples.append(self._nv.sm_mhz())
+        mask = self._nv.reasons()
+        for name, bit in _Nvml.REASONS:
+            if mask & bit:
                 self.reasons.add(name)
 
     def _loop(self):
@@ -164,7 +204,7 @@ class ClockSampler:
             self._t.join(timeout=5)
             try:
                 self._poll()
-                self._nv.nvmlShutdown()
+                self._nv.close()
             except Exception:
                 pass
 

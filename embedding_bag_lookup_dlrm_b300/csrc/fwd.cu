@@ -432,6 +432,7 @@ dlrm_status dispatch_types(int mode, const FwdArgs& a, int dtype, int index_type
 
 dlrm_status launch_forward(int mode, const FwdArgs& a, int dim, int dtype, int index_type, cudaStream_t s)
 {
+    if (forward_tc_supported(mode, dim, a.T, a.B, a.nnz)) return launch_forward_tc(mode, a, dim, dtype, index_type, s);
     switch (dim) {
         case 16: return dispatch_types<16>(mode, a, dtype, index_type, s);
         case 32: return dispatch_types<32>(mode, a, dtype, index_type, s);

@@ -38,6 +38,13 @@ struct FwdArgs {
 dlrm_status launch_forward(int mode, const FwdArgs& args, int dim, int dtype, int index_type,
                            cudaStream_t stream);
 
+// The same forward with the interaction on the tensor cores (fwd_tc.cu):
+// fused and interaction modes, D in {64, 128}, N = T + 1 <= 128, bags of
+// at most two lookups on average.
+bool forward_tc_supported(int mode, int dim, int num_tables, int64_t batch, int64_t nnz);
+dlrm_status launch_forward_tc(int mode, const FwdArgs& args, int dim, int dtype, int index_type,
+                              cudaStream_t stream);
+
 // ---- training step -------------------------------------------------------
 struct BwdArgs {
     float* tables[DLRM_MAX_TABLES];

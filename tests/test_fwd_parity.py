@@ -29,6 +29,13 @@ CASES = [
     (256, 40, "f32", "mean", "i32", 1, 3, 11),
     (16, 13, "bf16", "sum", "i32", 1, 70, 23),
     (64, 20, "bf16", "mean", "i32", 1, 1, 50),
+    # bags of 0..2 lookups: the tensor-core kernel, with its row-by-row pooling of the longer bags
+    (128, 26, "f32", "mean", "i32", 0, 2, 50),
+    (128, 26, "bf16", "sum", "i64", 0, 2, 37),
+    (64, 40, "bf16", "sum", "i64", 0, 2, 33),
+    (128, 100, "f32", "mean", "i32", 0, 2, 7),
+    (64, 63, "f32", "sum", "i32", 1, 1, 13),
+    (128, 31, "f32", "sum", "i32", 1, 1, 9),
 ]
 
 
@@ -84,15 +91,28 @@ def test_onehot_fp32_bit_exact(orc):
     assert np.array_equal(ps.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
-def test_identity_tables_exact_interaction():
-    """E_t = I: embedding-embedding values are [r_i == r_j], x-embedding values x[r_t], exactly."""
-    B, T, D = 64, 26, 128
+def _round_to_16_bits(x):
+    """x rounded to 16 significant bits: the sum of two bfloat16 values, which
+    is what the tensor-core Gram carries of each fp32 operand."""
+    hi = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(x))
+    lo = gen.bf16_bits_to_f32(gen.f32_to_bf16_bits((x - hi).astype(np.float32)))
+    return (hi + lo).astype(np.float32)
+
+
+@pytest.mark.parametrize("D,path", [(128, "tensor-core Gram"), (64, "tensor-core Gram"), (32, "FFMA Gram")])
+def test_identity_tables_exact_interaction(D, path):
+    """E_t = I: embedding-embedding values are [r_i == r_j], x-embedding values x[r_t], exactly.
+    The tensor-core path represents each operand as hi + lo (two bf16), so its
+    x is drawn with 16 significant bits; the FFMA path takes full fp32 x."""
+    B, T = 64, 26
     rng = np.random.default_rng(9)
     tabs = [np.eye(D, dtype=np.float32) for _ in range(T)]
     r = rng.integers(0, D, size=(T, B))
     r[:, 0] = 5  # one sample with every embedding equal
     idx, off = r.reshape(-1), np.arange(T * B + 1)
     x = rng.standard_normal((B, D)).astype(np.float32)
+    if path == "tensor-core Gram":
+        x = _round_to_16_bits(x)
     out = dl.dlrm_sparse_fwd(dev_tables(tabs, "f32"), dev_index(idx, "i32"), dev_index(off, "i32"),
                              torch.from_numpy(x).cuda()).cpu().numpy()
     iu = torch.triu_indices(T + 1, T + 1, offset=1).numpy()
@@ -102,10 +122,11 @@ def test_identity_tables_exact_interaction():
             assert out[b, D + k] == want
 
 
-@pytest.mark.parametrize("itype", ["i32", "i64"])
-def test_bad_inputs_flag_and_zero(itype, orc):
+@pytest.mark.parametrize("itype,Lmax", [("i32", 4), ("i64", 4), ("i32", 2)])
+def test_bad_inputs_flag_and_zero(itype, Lmax, orc):
+    """Bags of up to 4 lookups run on the register-pooling kernel, up to 2 on the tensor-core one."""
     B, T, D = 9, 3, 64
-    tabs, Vs, idx, off, dense = random_case(11, B, T, D, 20, 1, 4)
+    tabs, Vs, idx, off, dense = random_case(11, B, T, D, 20, 1, Lmax)
     idx[2] = 20        # == V: out of range
     idx[5] = -1
     idx[-1] = 1 << 30
