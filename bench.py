@@ -31,6 +31,8 @@ import numpy as np  # noqa: E402
 import gen  # noqa: E402
 
 METRIC = "sparse-forward samples/s and effective HBM GB/s (% of B300 peak) at 1 GPU"
+TRAIN_METRIC = ("sparse training-step samples/s (forward, interaction backward, sorted per-row gradient sums, "
+                "row-wise Adagrad) and effective HBM GB/s at 1 GPU")
 N_ROTATE = 8          # distinct pre-generated batches cycled through
 FLUSH_BYTES = 512 << 20  # > 4x the 126 MB L2
 
@@ -41,7 +43,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4])
+    p.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -74,6 +76,32 @@ def algorithmic_bytes(w: gen.Workload, batch: gen.Batch) -> int:
     the output, the indices and the offsets (int32)."""
     return (batch.nnz * w.D * w.elem_bytes + w.B * w.D * 4 + w.B * w.out_width * 4 + batch.nnz * 4
             + (w.T * w.B + 1) * 4)
+
+
+def sort_passes(w: gen.Workload) -> int:
+    """LSD radix passes of 8 bits over keys below the total row count."""
+    bits = 1
+    while (1 << bits) <= sum(w.num_rows):
+        bits += 1
+    return (bits + 7) // 8
+
+
+def train_bytes(w: gen.Workload, batch: gen.Batch) -> dict:
+    """Bytes one training step must move (int32 indices), by phase:
+    forward: looked-up rows, x, out, pooled vectors saved, indices, offsets;
+    backward: grad_out, x and pooled read, grad_dense written, dP written
+    once and read once per lookup, lookup keys written, (key, value) read
+    and written by each radix pass, and per touched row its weights and
+    accumulator read and written."""
+    nnz = batch.nnz
+    BTD = w.B * w.T * w.D * 4
+    off = batch.offsets.astype(np.int64)
+    touched = sum(int(np.unique(batch.indices[off[t * w.B]:off[(t + 1) * w.B]]).size) for t in range(w.T))
+    fwd = (nnz * w.D * w.elem_bytes + w.B * w.D * 4 + w.B * w.out_width * 4 + BTD + nnz * 4
+           + (w.T * w.B + 1) * 4)
+    bwd = (w.B * w.out_width * 4 + w.B * w.D * 4 + BTD + w.B * w.D * 4 + BTD + nnz * w.D * 4 + nnz * 8
+           + sort_passes(w) * nnz * 16 + touched * (2 * w.D * 4 + 8) + nnz * 4 + (w.T * w.B + 1) * 4)
+    return {"forward": fwd, "backward": bwd, "total": fwd + bwd, "touched_rows": touched}
 
 
 def peaks():
@@ -219,63 +247,88 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle as it stands, on host cores
 # ---------------------------------------------------------------------------
+def sub_batch(w: gen.Workload, b: gen.Batch, S: int):
+    """The first S samples of a batch (all their bags), as a workload of batch S."""
+    import dataclasses
+    S = min(S, w.B)
+    off = b.offsets.astype(np.int64)
+    L = np.diff(off).reshape(w.T, w.B)[:, :S]
+    new_off = np.zeros(w.T * S + 1, np.int64)
+    np.cumsum(L.reshape(-1), out=new_off[1:])
+    idx = np.concatenate([b.indices[off[t * w.B]:off[t * w.B] + L[t].sum()] for t in range(w.T)])
+    g = b.grad_out[:S] if b.grad_out is not None else None
+    return (dataclasses.replace(w, B=S),
+            gen.Batch(indices=idx.astype(np.int32), offsets=new_off.astype(np.int32), dense=b.dense[:S], grad_out=g))
+
+
+class OracleStep:
+    """One step of the path on the CPU oracle (plain C, OpenMP over samples):
+    the fused forward, and for training also the interaction backward, the
+    per-row gradient sums and row-wise Adagrad.  Tables are host copies of the
+    rows the batch touches."""
+
+    def __init__(self, w: gen.Workload, b: gen.Batch):
+        import oracle
+        self.orc = oracle.get()
+        self.w, self.b = w, b
+        self.tabs, self.nr, self.idx = gen.compact_tables(w, b)
+        if w.train:
+            self.acc = [np.full(n, w.accum_init, np.float32) for n in self.nr]
+
+    def __call__(self):
+        w, b = self.w, self.b
+        r = self.orc.sparse_fwd(self.tabs, self.nr, self.idx, b.offsets, b.dense, w.mode, w.dtype,
+                                with_pooled=w.train)
+        if w.train:
+            self.orc.sparse_bwd_adagrad(self.tabs, self.nr, self.idx, b.offsets, b.dense, r["pooled"], b.grad_out,
+                                        self.acc, w.lr, w.eps, w.mode)
+
+
 def oracle_baseline(w: gen.Workload, batch: gen.Batch, seconds: float):
-    """Time the oracle's sparse forward on whole batches of the workload until
-    `seconds` have passed.  Tables: host copies of the rows the batch touches."""
-    import oracle
-    orc = oracle.get()
-    tabs, nr, cidx = gen.compact_tables(w, batch)
+    """Time the oracle on the workload until `seconds` have passed: whole
+    batches for the forward, a 4096-sample part of one for the training step."""
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    orc.sparse_fwd(tabs, nr, cidx, batch.offsets, batch.dense, w.mode, w.dtype)  # warm
+    if w.train:
+        ws, bs = sub_batch(w, batch, 4096)
+        what = f"first {ws.B} samples of one batch"
+    else:
+        ws, bs = w, batch
+        what = f"one full batch of {w.B} samples"
+    run = OracleStep(ws, bs)
+    run()  # warm
     n, t0 = 0, time.perf_counter()
     while True:
-        orc.sparse_fwd(tabs, nr, cidx, batch.offsets, batch.dense, w.mode, w.dtype)
+        run()
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": n * w.B / el, "unit": "samples/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} x one full batch of {w.B} samples (rows the batch touches copied to host memory), "
-                      f"{el:.1f} s"}
+    return {"value": n * ws.B / el, "unit": "samples/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} x {what} (rows the batch touches copied to host memory), {el:.1f} s"}
 
 
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle
-    orc = oracle.get()
     batches = gen.make_batches(w, range(min(N_ROTATE, max(1, args.steps))))
-    prepared = [(b, gen.compact_tables(w, b)) for b in batches]
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    # each step: a bounded sample of the batch (first S samples) sized to ~1-2 s
-    S = min(w.B, 16384)
-
-    def sub(b, tabs_nr_idx, S):
-        tabs, nr, cidx = tabs_nr_idx
-        off = b.offsets.astype(np.int64)
-        L = np.diff(off).reshape(w.T, w.B)[:, :S]
-        new_off = np.zeros(w.T * S + 1, np.int64)
-        np.cumsum(L.reshape(-1), out=new_off[1:])
-        idx = np.concatenate([cidx[off[t * w.B]:off[t * w.B] + L[t].sum()] for t in range(w.T)])
-        return tabs, nr, idx, new_off, b.dense[:S]
-
-    subs = [sub(b, p, S) for b, p in prepared]
+    # each step: a bounded sample of one batch (its first S samples), about a second of CPU work
+    S = min(w.B, 4096 if w.train else 16384)
+    runs = [OracleStep(*sub_batch(w, b, S)) for b in batches]
     for i in range(args.warmup):
-        tabs, nr, idx, off, x = subs[i % len(subs)]
-        orc.sparse_fwd(tabs, nr, idx, off, x, w.mode, w.dtype)
+        runs[i % len(runs)]()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        tabs, nr, idx, off, x = subs[i % len(subs)]
-        orc.sparse_fwd(tabs, nr, idx, off, x, w.mode, w.dtype)
+        runs[i % len(runs)]()
     el = time.perf_counter() - t0
     value = args.steps * S / el
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded generator)", "config": config_of(w, args),
+    line = {"impl": "reference", "metric": TRAIN_METRIC if w.train else METRIC, "value": value,
+            "unit": "samples/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded generator)", "config": config_of(w, args),
             "cpu_baseline": {"value": value, "unit": "samples/s", "cores": cores, "kind": "oracle",
-                             "sample": f"each step: first {S} samples of one of {len(subs)} rotated batches; "
+                             "sample": f"each step: first {S} samples of one of {len(runs)} rotated batches; "
                                        "rows the batch touches copied to host memory"},
             "e2e": {"value": value, "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -320,11 +373,28 @@ def run_ours(args, w):
     dev_batches = [tuple(torch.from_numpy(a).to(dev) for a in (b.indices, b.offsets, b.dense)) for b in batches]
     out = torch.empty((w.B, w.out_width), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if w.train:
+        accum = [torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+        grads = [torch.from_numpy(b.grad_out).to(dev) for b in batches]
+        pooled = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device=dev)
+        grad_dense = torch.empty((w.B, w.D), dtype=torch.float32, device=dev)
+        ws_bytes = max(dl.dlrm_sparse_bwd_workspace_size(tables, torch.from_numpy(b.indices), torch.from_numpy(b.offsets))
+                       for b in batches)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    def step(i, s):
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def step(i, s, mid=None):
         idx, off, x = dev_batches[i % N_ROTATE]
-        dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, stream=s)
+        if not w.train:
+            dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, stream=s)
+            return
+        dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, pooled_save=pooled, stream=s)
+        if mid is not None:
+            mid.record(s)
+        dl.dlrm_sparse_bwd_adagrad(tables, accum, idx, off, x, pooled, grads[i % N_ROTATE], w.lr, w.eps, w.mode,
+                                   grad_dense=grad_dense, workspace=workspace, stream=s)
 
     s = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(s):
@@ -337,14 +407,17 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # kernels of one step: the fused forward, and for training the backward's
+    # interaction, key fill and expansion, 3 per radix pass, 2 for the row updates
+    per_step = 1 + ((5 + 3 * sort_passes(w)) if w.train else 0)
     launches = 0
     with ClockSampler(local) as clk, torch.cuda.stream(s):
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()                      # evict L2 (outside the timed events)
             starts[i].record(s)
-            step(args.warmup + i, s)
-            launches += 1                      # one fused kernel per step
+            step(args.warmup + i, s, mids[i])
+            launches += per_step
             ends[i].record(s)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -355,38 +428,148 @@ def run_ours(args, w):
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     value = w.B * world * args.steps / (total_ms / 1e3)
-
-    # roofline of the fused kernel (the step is that one kernel)
-    alg = statistics.mean(algorithmic_bytes(w, b) for b in batches)
-    kernel_ms = statistics.mean(step_ms)
-    achieved = alg / (kernel_ms / 1e3) / 1e9
     peak, src = peaks()
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic_for(args.workload),
-            "kernel": "forward_kernel (fused sparse forward)", "peak_source": f"{src} (hbm_gbs)",
-            "algorithmic_bytes_per_launch": int(alg), "frac_of_nominal_8000": round(achieved / 8000.0, 4),
-            "median_launch_ms": round(statistics.median(step_ms), 4)}
 
-    # end to end: pinned host inputs -> device -> fused forward -> output to host
+    if not w.train:
+        # roofline of the fused kernel (the step is that one kernel)
+        alg = statistics.mean(algorithmic_bytes(w, b) for b in batches)
+        kernel_ms = statistics.mean(step_ms)
+        achieved = alg / (kernel_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic_for(args.workload),
+                "kernel": forward_kernel_name(w), "peak_source": f"{src} (hbm_gbs, burst copy)",
+                "algorithmic_bytes_per_launch": int(alg), "frac_of_nominal_8000": round(achieved / 8000.0, 4),
+                "median_launch_ms": round(statistics.median(step_ms), 4)}
+        effective = achieved
+    else:
+        tb = [train_bytes(w, b) for b in batches]
+        fwd_ms = [a.elapsed_time(m) for a, m in zip(starts, mids)]
+        bwd_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+        fwd_b = statistics.mean(t["forward"] for t in tb)
+        bwd_b = statistics.mean(t["backward"] for t in tb)
+        tot_b = fwd_b + bwd_b
+        effective = tot_b / (statistics.mean(step_ms) / 1e3) / 1e9
+        fwd_gbs = fwd_b / (statistics.mean(fwd_ms) / 1e3) / 1e9
+        bwd_gbs = bwd_b / (statistics.mean(bwd_ms) / 1e3) / 1e9
+        dom = "backward" if statistics.mean(bwd_ms) >= statistics.mean(fwd_ms) else "forward"
+        ach = bwd_gbs if dom == "backward" else fwd_gbs
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "traffic": traffic_for(args.workload),
+                "kernel": ("dlrm_sparse_bwd_adagrad kernels (interaction backward, keys, radix sort, row updates)"
+                           if dom == "backward" else forward_kernel_name(w)),
+                "peak_source": f"{src} (hbm_gbs, burst copy)",
+                "algorithmic_bytes_per_launch": int(bwd_b if dom == "backward" else fwd_b),
+                "phases": {"forward_ms": round(statistics.mean(fwd_ms), 4), "forward_gbs": round(fwd_gbs, 1),
+                           "forward_bytes": int(fwd_b), "backward_ms": round(statistics.mean(bwd_ms), 4),
+                           "backward_gbs": round(bwd_gbs, 1), "backward_bytes": int(bwd_b),
+                           "touched_rows": int(statistics.mean(t["touched_rows"] for t in tb))},
+                "step_effective_gbs": round(effective, 1), "step_frac": round(effective / peak, 4)}
+
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, tables, batches, dev, dl, torch, world)
+        e2e = (run_e2e_train(args, w, tables, batches, dev, dl, torch, world) if w.train
+               else run_e2e(args, w, tables, batches, dev, dl, torch, world))
 
     cpu = None
     if rank == 0 and not args.no_cpu and world == 1:
         cpu = oracle_baseline(w, batches[0], args.cpu_seconds)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 1), "unit": "samples/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        line = {"metric": TRAIN_METRIC if w.train else METRIC, "value": round(value, 1), "unit": "samples/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded generator, tables filled on device)", "config": config_of(w, args),
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk.summary(), "wall_s_timed_region": round(t_wall, 3),
-                "effective_gbs": round(achieved, 1)}
+                "effective_gbs": round(effective, 1)}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def forward_kernel_name(w):
+    """Which forward kernel the library picks for this workload (mirrors its dispatch)."""
+    tc = w.D in (64, 128) and w.T + 1 <= 128 and (w.bag_max + w.bag_min) / 2 <= 2
+    return ("forward_tc_kernel (fused sparse forward, tcgen05 Gram)" if tc
+            else "forward_kernel (fused sparse forward, FFMA Gram)")
+
+
+def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):
+    """Training steps fed from pinned host memory: indices, offsets, dense and
+    grad_out copied in on a copy stream (the next step's copies overlap this
+    step's kernels), grad_dense copied back, all inside the timed region."""
+    host = [tuple(torch.from_numpy(a).pin_memory() for a in (b.indices, b.offsets, b.dense, b.grad_out))
+            for b in batches]
+    max_nnz = max(b.nnz for b in batches)
+    comp, copy = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    stages = []
+    for _ in range(2):
+        stages.append((torch.empty(max_nnz, dtype=torch.int32, device=dev),
+                       torch.empty(w.T * w.B + 1, dtype=torch.int32, device=dev),
+                       torch.empty((w.B, w.D), dtype=torch.float32, device=dev),
+                       torch.empty((w.B, w.out_width), dtype=torch.float32, device=dev)))
+    accum = [torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+    pooled = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.out_width), dtype=torch.float32, device=dev)
+    gd = torch.empty((w.B, w.D), dtype=torch.float32, device=dev)
+    gd_host = [torch.empty((w.B, w.D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    ws = torch.empty(max(dl.dlrm_sparse_bwd_workspace_size(tables, torch.from_numpy(b.indices), torch.from_numpy(b.offsets))
+                         for b in batches),
+                     dtype=torch.uint8, device=dev)
+    copied = [None, None]
+    used = [None, None]
+
+    def h2d(i):
+        k = i % 2
+        hi, ho, hx, hg = host[i % N_ROTATE]
+        di, do, dx, dg = stages[k]
+        with torch.cuda.stream(copy):
+            if used[k] is not None:
+                copy.wait_event(used[k])
+            di[:hi.numel()].copy_(hi, non_blocking=True)
+            do.copy_(ho, non_blocking=True)
+            dx.copy_(hx, non_blocking=True)
+            dg.copy_(hg, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy)
+            copied[k] = ev
+
+    def run(i):
+        k = i % 2
+        hi = host[i % N_ROTATE][0]
+        di, do, dx, dg = stages[k]
+        comp.wait_event(copied[k])
+        dl.dlrm_sparse_fwd(tables, di[:hi.numel()], do, dx, w.mode, out=out, pooled_save=pooled, stream=comp)
+        dl.dlrm_sparse_bwd_adagrad(tables, accum, di[:hi.numel()], do, dx, pooled, dg, w.lr, w.eps, w.mode,
+                                   grad_dense=gd, workspace=ws, stream=comp)
+        with torch.cuda.stream(comp):
+            gd_host[k].copy_(gd, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(comp)
+        used[k] = ev
+
+    def steps(first, count):
+        h2d(first)
+        for i in range(first, first + count):
+            if i + 1 < first + count:
+                h2d(i + 1)
+            run(i)
+
+    steps(0, args.warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    t0 = time.perf_counter()
+    steps(args.warmup, args.steps)
+    torch.cuda.synchronize()
+    el = max_over_ranks(time.perf_counter() - t0, world)
+    h2d_b = int(np.mean([b.indices.nbytes + b.offsets.nbytes + b.dense.nbytes + b.grad_out.nbytes for b in batches]))
+    return {"value": round(w.B * world * args.steps / el, 1), "unit": "samples/s", "h2d_bytes_per_step": h2d_b,
+            "d2h_bytes_per_step": w.B * w.D * 4, "ms_per_step": round(el / args.steps * 1e3, 4),
+            "how": "indices, offsets, dense, grad_out from pinned host memory on a copy stream (next step's copies "
+                   "overlap this step's kernels); fused forward + training step; grad_dense back to pinned host; "
+                   "wall clock over the timed steps"}
 
 
 def run_e2e(args, w, tables, batches, dev, dl, torch, world):
