@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--max-rows", type=int, default=0,
                    help="cap every table at this many rows (a small case of the same kernel, for profiling)")
+    p.add_argument("--batch", type=int, default=0,
+                   help="override the batch size (a small case of the same kernels, for profiling)")
     p.add_argument("--uniform", action="store_true",
                    help="uniform instead of Zipf indices (every lookup a likely DRAM read)")
     return p.parse_args()
@@ -621,6 +623,9 @@ def main():
     if args.max_rows > 0:
         w.num_rows = [min(v, args.max_rows) for v in w.num_rows]
         w.name += f" [tables capped at {args.max_rows} rows]"
+    if args.batch > 0:
+        w.B = args.batch
+        w.name += f" [batch {args.batch}]"
     if args.uniform:
         w.index_dist = "uniform"
         w.name += " [uniform indices]"

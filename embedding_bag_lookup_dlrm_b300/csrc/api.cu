@@ -217,6 +217,7 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* 
     a.mean = mode == DLRM_POOL_MEAN;
     a.lr = lr;
     a.eps = eps;
+    a.t_magic = a.T >= 2 ? ~uint64_t{0} / static_cast<uint64_t>(a.T) + 1 : 0;
     return dlrm::launch_backward(a, tables->dim, bags->index_type, workspace, workspace_bytes, stream);
 }
 

@@ -27,7 +27,8 @@ constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;  // 4096 keys per tile
 constexpr int kRadixBits = 8;
 constexpr int kBins = 1 << kRadixBits;
-constexpr int kChunk = 256;  // sorted lookups per segment-reduction warp
+constexpr int kChunk = 128;  // sorted lookups per segment-reduction warp
+constexpr int kSegThreads = 128;
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
 
@@ -110,7 +111,9 @@ __host__ __device__ inline BwdLayout make_bwd_layout(int T, int D)
     return l;
 }
 
-template <int D, int G>
+// In mean mode dP[b][t] is stored already divided by the bag length L (the
+// scale every lookup of the bag applies), so the per-row sums are plain sums.
+template <int D, int G, typename TI>
 __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant__ BwdArgs a, float* __restrict__ dP,
                                                            int groups_per_cta)
 {
@@ -200,7 +203,17 @@ __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant
                     u.w = go[col + 3] + acc[0].w;
                     *reinterpret_cast<float4*>(a.grad_dense + b * D + col) = u;
                 } else {
-                    *reinterpret_cast<float4*>(dP + (b * T + (i - 1)) * D + col) = acc[r];
+                    float4 u = acc[r];
+                    if (a.mean) {
+                        const int64_t bag = static_cast<int64_t>(i - 1) * a.B + b;
+                        const int64_t L = ld_index<TI>(a.offsets, bag + 1) - ld_index<TI>(a.offsets, bag);
+                        if (L > 0) {
+                            const float fl = static_cast<float>(L);
+                            u = make_float4(__fdiv_rn(u.x, fl), __fdiv_rn(u.y, fl), __fdiv_rn(u.z, fl),
+                                            __fdiv_rn(u.w, fl));
+                        }
+                    }
+                    *reinterpret_cast<float4*>(dP + (b * T + (i - 1)) * D + col) = u;
                 }
             }
         }
@@ -431,15 +444,61 @@ __device__ __forceinline__ void adagrad_row(const BwdArgs& a, uint32_t key, int 
     if (lane == 0) *acc = A;
 }
 
-template <int D, typename TI>
-__global__ void __launch_bounds__(256) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
-                                                            const uint32_t* __restrict__ keys,
-                                                            const uint32_t* __restrict__ vals,
-                                                            const float* __restrict__ dP,
-                                                            float* __restrict__ partial, int64_t num_chunks)
+// t = v / T for v < 2^32, with magic = ceil(2^64 / T) (T >= 2): the product's
+// high word (Granlund & Montgomery's division by invariant integers).
+__device__ __forceinline__ uint32_t div_by_T(uint32_t v, const BwdArgs& a)
+{
+    return a.T == 1 ? v : static_cast<uint32_t>(__umul64hi(static_cast<uint64_t>(v), a.t_magic));
+}
+
+// Row-wise Adagrad on one row whose weights (this lane's slice) and
+// accumulator were read earlier: w is the row before the step, acc_old its
+// accumulator.
+template <int D>
+__device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, int t,
+                                              const float4 (&g)[Lanes<D>::kChunks],
+                                              const float4 (&w)[Lanes<D>::kChunks], float acc_old, int lane)
 {
     constexpr int C = Lanes<D>::kChunks;
-    constexpr int U = 8;
+    const bool active = lane < Lanes<D>::kActive;
+    float ss = 0.0f;
+    if (active) {
+#pragma unroll
+        for (int k = 0; k < C; ++k) ss += g[k].x * g[k].x + g[k].y * g[k].y + g[k].z * g[k].z + g[k].w * g[k].w;
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
+    const int64_t r = static_cast<int64_t>(key) - a.row_base[t];
+    const float A = acc_old + ss / static_cast<float>(D);
+    const float den = sqrtf(A) + a.eps;
+    if (active) {
+        float* wr = a.tables[t] + r * D;
+#pragma unroll
+        for (int k = 0; k < C; ++k) {
+            float4 v = w[k];
+            v.x -= a.lr * g[k].x / den;
+            v.y -= a.lr * g[k].y / den;
+            v.z -= a.lr * g[k].z / den;
+            v.w -= a.lr * g[k].w / den;
+            *reinterpret_cast<float4*>(wr + (lane + k * kWarp) * 4) = v;
+        }
+    }
+    if (lane == 0) a.accum[t][r] = A;
+}
+
+// Per group of U sorted lookups the warp issues, together, the loads of the
+// group's dP rows and of the weights and accumulator of every row whose run
+// starts in the group (each row is updated once per call, so reading it early
+// is safe), then walks the group in order.
+template <int D>
+__global__ void __launch_bounds__(kSegThreads, 4) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
+                                                                       const uint32_t* __restrict__ keys,
+                                                                       const uint32_t* __restrict__ vals,
+                                                                       const float* __restrict__ dP,
+                                                                       float* __restrict__ partial, int64_t num_chunks)
+{
+    constexpr int C = Lanes<D>::kChunks;
+    constexpr int U = 8;  // lookups per group
     const int lane = threadIdx.x & 31;
     const int64_t chunk = blockIdx.x * int64_t{blockDim.x / kWarp} + (threadIdx.x >> 5);
     if (chunk >= num_chunks) return;
@@ -452,16 +511,17 @@ __global__ void __launch_bounds__(256) segment_chunk_kernel(const __grid_constan
     uint32_t cur = kSentinel;
     int cur_t = 0;
     bool cur_first = true;  // current run is the chunk's first run
-    float4 g[C];
+    float4 g[C], cw[C];     // the run's gradient sum; its row's weights (read at the run's start)
+    float ca = 0.0f;        // its accumulator
 #pragma unroll
-    for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < C; ++k) g[k] = cw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
     auto flush = [&]() {
         if (cur == kSentinel) return;
         const bool cut_before = cur_first && before_key == cur;
         const bool cut_after = after_key == cur;
         if (!cut_before && !cut_after) {
-            adagrad_row<D>(a, cur, cur_t, g, lane);
+            adagrad_apply<D>(a, cur, cur_t, g, cw, ca, lane);
         } else {
             float* dst = partial + ((chunk * 2) + (cur_first ? 0 : 1)) * D;
             if (active) {
@@ -471,37 +531,45 @@ __global__ void __launch_bounds__(256) segment_chunk_kernel(const __grid_constan
         }
     };
 
+    uint32_t prev_key = before_key;  // key of the lookup before the current group
     for (int64_t base = c0; base < c1; base += kWarp) {
         const int64_t p = base + lane;
         const uint32_t kk = p < c1 ? keys[p] : kSentinel;
         const uint32_t vv = p < c1 ? vals[p] : 0u;
         const int nq = static_cast<int>(c1 - base < kWarp ? c1 - base : kWarp);
         for (int j0 = 0; j0 < nq; j0 += U) {
-            float4 row[U][C];
+            float4 row[U][C], wp[U][C];
+            float ap[U];
             uint32_t kj[U];
-            float sc[U];
             int tj[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int j = j0 + u;
                 kj[u] = __shfl_sync(0xffffffffu, kk, j & 31);
                 const uint32_t vj = __shfl_sync(0xffffffffu, vv, j & 31);
-                const bool live = j < nq && kj[u] != kSentinel;
-                if (!live) kj[u] = kSentinel;
-                tj[u] = static_cast<int>(vj % static_cast<uint32_t>(a.T));
-                sc[u] = 1.0f;
-                if (live && a.mean) {
-                    const int64_t b = vj / static_cast<uint32_t>(a.T);
-                    const int64_t bag = static_cast<int64_t>(tj[u]) * a.B + b;
-                    const int64_t L = ld_index<TI>(a.offsets, bag + 1) - ld_index<TI>(a.offsets, bag);
-                    sc[u] = 1.0f / static_cast<float>(L);
-                }
-                if (live && active) {
-                    const float* src = dP + static_cast<int64_t>(vj) * D;
+                if (j >= nq) kj[u] = kSentinel;
+                const uint32_t kprev = u == 0 ? prev_key : kj[u - 1];
+                tj[u] = 0;
+                if (kj[u] != kSentinel) {
+                    if (active) {
+                        const float* src = dP + static_cast<int64_t>(vj) * D;
 #pragma unroll
-                    for (int k = 0; k < C; ++k) row[u][k] = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
+                        for (int k = 0; k < C; ++k) row[u][k] = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
+                    }
+                    if (kj[u] != kprev) {  // a run starts here: read its row now
+                        const uint32_t b = div_by_T(vj, a);
+                        tj[u] = static_cast<int>(vj - b * static_cast<uint32_t>(a.T));
+                        const int64_t r = static_cast<int64_t>(kj[u]) - a.row_base[tj[u]];
+                        ap[u] = a.accum[tj[u]][r];
+                        if (active) {
+                            const float* wr = a.tables[tj[u]] + r * D;
+#pragma unroll
+                            for (int k = 0; k < C; ++k) wp[u][k] = *reinterpret_cast<const float4*>(wr + (lane + k * kWarp) * 4);
+                        }
+                    }
                 }
             }
+            prev_key = kj[U - 1] != kSentinel ? kj[U - 1] : prev_key;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (kj[u] == kSentinel) continue;
@@ -510,16 +578,20 @@ __global__ void __launch_bounds__(256) segment_chunk_kernel(const __grid_constan
                     cur_first = (cur == kSentinel);
                     cur = kj[u];
                     cur_t = tj[u];
+                    ca = ap[u];
 #pragma unroll
-                    for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < C; ++k) {
+                        g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        cw[k] = wp[u][k];
+                    }
                 }
                 if (active) {
 #pragma unroll
                     for (int k = 0; k < C; ++k) {
-                        g[k].x = fmaf(row[u][k].x, sc[u], g[k].x);
-                        g[k].y = fmaf(row[u][k].y, sc[u], g[k].y);
-                        g[k].z = fmaf(row[u][k].z, sc[u], g[k].z);
-                        g[k].w = fmaf(row[u][k].w, sc[u], g[k].w);
+                        g[k].x += row[u][k].x;
+                        g[k].y += row[u][k].y;
+                        g[k].z += row[u][k].z;
+                        g[k].w += row[u][k].w;
                     }
                 }
             }
@@ -530,7 +602,7 @@ __global__ void __launch_bounds__(256) segment_chunk_kernel(const __grid_constan
 
 // One warp per chunk that holds the start of a run cut by its end border.
 template <int D>
-__global__ void __launch_bounds__(256) segment_span_kernel(const __grid_constant__ BwdArgs a,
+__global__ void __launch_bounds__(kSegThreads) segment_span_kernel(const __grid_constant__ BwdArgs a,
                                                            const uint32_t* __restrict__ keys,
                                                            const uint32_t* __restrict__ vals,
                                                            const float* __restrict__ partial, int64_t num_chunks)
@@ -578,7 +650,7 @@ __global__ void __launch_bounds__(256) segment_span_kernel(const __grid_constant
 // ---------------------------------------------------------------------------
 constexpr int kMaxSmem = 227 * 1024;
 
-template <int D, int G>
+template <int D, int G, typename TI>
 dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
 {
     const BwdLayout l = make_bwd_layout(a.T, D);
@@ -591,7 +663,7 @@ dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
         return DLRM_ERR_UNSUPPORTED;
     }
     const size_t smem = static_cast<size_t>(groups) * l.bytes;
-    auto kern = interact_bwd_kernel<D, G>;
+    auto kern = interact_bwd_kernel<D, G, TI>;
     if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
         return DLRM_ERR_CUDA;
     const int64_t blocks = (a.B + groups - 1) / groups;
@@ -604,7 +676,7 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
 {
     // interaction backward: a sample's g V is shared by 8 warps for wide N
     const int nblk = round_up(a.T + 1, 8) / 8;
-    dlrm_status st = nblk > 8 ? launch_interact_bwd<D, 8>(a, w.dP, s) : launch_interact_bwd<D, 1>(a, w.dP, s);
+    dlrm_status st = nblk > 8 ? launch_interact_bwd<D, 8, TI>(a, w.dP, s) : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
     if (st != DLRM_OK) return st;
     if (a.nnz == 0) return DLRM_OK;
 
@@ -626,10 +698,10 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
             w.bin_total);
         cur ^= 1;
     }
-    const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + 7) / 8);
-    segment_chunk_kernel<D, TI><<<seg_blocks, 256, 0, s>>>(a, w.keys[cur], w.vals[cur], w.dP, w.partial,
-                                                           w.num_chunks);
-    segment_span_kernel<D><<<seg_blocks, 256, 0, s>>>(a, w.keys[cur], w.vals[cur], w.partial, w.num_chunks);
+    const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + kSegThreads / kWarp - 1) / (kSegThreads / kWarp));
+    segment_chunk_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], w.dP, w.partial,
+                                                               w.num_chunks);
+    segment_span_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], w.partial, w.num_chunks);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 

@@ -64,6 +64,7 @@ struct BwdArgs {
     int32_t mean;
     float lr;
     float eps;
+    uint64_t t_magic;  // ceil(2^64 / T) for T >= 2: sort value v = b*T + t gives b = high word of v * t_magic
 };
 
 size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz);
