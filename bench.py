@@ -514,9 +514,12 @@ def run_ours(args, w):
 
 def forward_kernel_name(w):
     """Which forward kernel the library picks for this workload (mirrors its dispatch)."""
-    tc = w.D in (64, 128) and w.T + 1 <= 128 and (w.bag_max + w.bag_min) / 2 <= 2
-    return ("forward_tc_kernel (fused sparse forward, tcgen05 Gram)" if tc
-            else "forward_kernel (fused sparse forward, FFMA Gram)")
+    mean_len = (w.bag_max + w.bag_min) / 2
+    tc = w.D in (64, 128) and w.T + 1 <= 128 and mean_len <= 16
+    if not tc:
+        return "forward_kernel (fused sparse forward, FFMA Gram)"
+    return ("forward_tc_kernel (fused sparse forward, tcgen05 Gram"
+            + (", multi-lookup bags)" if mean_len > 1.25 else ")"))
 
 
 def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):

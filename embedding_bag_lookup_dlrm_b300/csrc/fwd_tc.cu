@@ -287,7 +287,9 @@ __device__ __forceinline__ int pop_rows(uint32_t& mask, int g)
     return mine;
 }
 
-template <int D, typename TE, typename TI, int MODE, int NP>
+// MULTI: bags of several lookups are pooled by the whole warp from one list of
+// lookups (else one bag at a time, the rare case of a mostly one-hot batch).
+template <int D, typename TE, typename TI, int MODE, int NP, bool MULTI>
 __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_constant__ FwdArgs a, int64_t num_tiles)
 {
     constexpr int C = D / kWarp;                 // columns per lane when pooling in registers
@@ -407,9 +409,91 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
         const RowMeta<TI> m_next = stage_bag<TI, MODE, NP>(a, tile + G, num_tiles, warp, lane, o_next);
         o_next = load_offsets<TI, MODE, NP>(a, tile + 2 * G, num_tiles, warp, lane);
 
-        // ---- empty bags (or a lone index out of range) pool to zero ----
+        // ---- bags of several lookups: the warp's lookups as one list, 16 rows in flight, each summed
+        //      in lookup order in registers; a finished sum goes to its row's lines as an fp32 row ----
+        uint32_t multi = 0, pooled_rows = 0, zero_rows = 0;
+        if (MODE == kFused && MULTI) multi = __ballot_sync(kFull, m.len > 1);
+        if (MULTI && multi != 0) {
+            using Slice4 = Slice<4 * static_cast<int>(sizeof(TE))>;
+            const bool lane_on = lane < F32_CHUNKS;  // lane l sums elements 4l .. 4l + 3
+            const int lenm = ((multi >> lane) & 1u) ? m.len : 0;
+            int incl = lenm;
+#pragma unroll
+            for (int o = 1; o < kWarp; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int total = __shfl_sync(kFull, incl, kWarp - 1);
+            uint32_t started = 0;  // rows that received a valid lookup
+            int cur = -1;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            auto store_cur = [&]() {
+                if (cur >= 0 && ((started >> cur) & 1u) && lane_on)
+                    *reinterpret_cast<float4*>(op_hi + (lane >> 3) * REGION + (kWarp * warp + cur) * 128 + (lane & 7) * 16) = acc;
+            };
+            for (int q0 = 0; q0 < total; q0 += kWarp) {
+                // lane l resolves lookup q = q0 + l: its row is the number of rows whose list ends at or before q
+                const int q = q0 + lane;
+                int r = 0;
+#pragma unroll
+                for (int bit = 16; bit > 0; bit >>= 1) {
+                    const int e = __shfl_sync(kFull, incl, r + bit - 1);
+                    if (e <= q) r += bit;
+                }
+                const int rs = r & (kWarp - 1);
+                const int beg = __shfl_sync(kFull, incl - lenm, rs);
+                const int64_t st = static_cast<int64_t>(__shfl_sync(kFull, static_cast<long long>(m.start), rs));
+                const char* src = nullptr;
+                if (q < total) {
+                    const int t_r = (kWarp * warp + r) % NP - 1;
+                    const int64_t idx = load_idx<TI>(a.indices, st + (q - beg));
+                    if (idx >= 0 && idx < tab_rows[t_r])
+                        src = tab_base[t_r] + static_cast<uint64_t>(idx) * TE_BYTES;
+                    else
+                        flag_status(a.status, DLRM_ERR_INDEX_OOB);  // contributes zero, still counts in L
+                }
+                const uint32_t vmask = __ballot_sync(kFull, src != nullptr);
+#pragma unroll 1
+                for (int h = 0; h < kWarp; h += 16) {
+                    if (q0 + h >= total) break;
+                    Slice4 raw[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const char* p = reinterpret_cast<const char*>(shfl64(reinterpret_cast<int64_t>(src), h + u));
+                        if (p != nullptr && lane_on) raw[u].load(p, lane);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        if (q0 + h + u >= total) break;
+                        const int ru = __shfl_sync(kFull, r, h + u);
+                        if (ru != cur) {
+                            store_cur();
+                            cur = ru;
+                        }
+                        if ((vmask >> (h + u)) & 1u) {
+                            float f[4];
+                            widen<4, TE>(raw[u], f);
+                            if ((started >> cur) & 1u) {
+                                acc.x += f[0];
+                                acc.y += f[1];
+                                acc.z += f[2];
+                                acc.w += f[3];
+                            } else {  // a sum starts from its first term
+                                acc = make_float4(f[0], f[1], f[2], f[3]);
+                                started |= 1u << cur;
+                            }
+                        }
+                    }
+                }
+            }
+            store_cur();
+            pooled_rows = started;
+            zero_rows = multi & ~started;  // every lookup out of range: the bag pools to zero
+        }
+
+        // ---- empty bags (or bags whose every index is out of range) pool to zero ----
         {
-            uint32_t mask = empty;
+            uint32_t mask = empty | zero_rows;
             const int g = lane / F32_CHUNKS, gl = lane % F32_CHUNKS;
             while (mask != 0) {
                 const int r = pop_rows<F32_GROUPS>(mask, g);
@@ -425,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
         }
 
         // ---- rows of longer bags, one at a time: 8 lookups in flight, summed in lookup order ----
-        if (MODE == kFused) {
+        if (MODE == kFused && !MULTI) {
             uint32_t multi = __ballot_sync(kFull, m.len > 1);
             while (multi != 0) {
                 const int rr = __ffs(multi) - 1;
@@ -485,21 +569,32 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
         __syncwarp();
         {
             {
-                // lane group g32 splits rows g32 * F32_SLOTS + q, four at a time: loads first, then the math
+                // lane group g32 splits rows g32 * F32_SLOTS + q, four at a time: loads first, then the math.
+                // A pooled bag of a mean-pooled table is divided by its length here.
+                const uint32_t conv_rows = conv_f32 | pooled_rows;
                 const bool x_warp = i0 == 0 && (conv_f32 & 1u);  // row 0 of this warp is a dense vector x
+                const bool scale = mean && pooled_rows != 0;
 #pragma unroll
                 for (int q0 = 0; q0 < F32_SLOTS; q0 += 4) {
                     float4 v[4];
+                    int Lq[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if ((conv_f32 >> (g32 * F32_SLOTS + q0 + q)) & 1u)
+                    for (int q = 0; q < 4; ++q) {
+                        Lq[q] = scale ? __shfl_sync(kFull, m.len, g32 * F32_SLOTS + q0 + q) : 1;
+                        if ((conv_rows >> (g32 * F32_SLOTS + q0 + q)) & 1u)
                             v[q] = *reinterpret_cast<const float4*>(raw_lane + (q0 + q) * 128);
+                    }
                     __syncwarp();
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int r = g32 * F32_SLOTS + q0 + q;
-                        if (!((conv_f32 >> r) & 1u)) continue;
+                        if (!((conv_rows >> r) & 1u)) continue;
                         const int row = kWarp * warp + r;
+                        if (scale && ((pooled_rows >> r) & 1u)) {
+                            const float fl = static_cast<float>(Lq[q]);
+                            v[q] = make_float4(__fdiv_rn(v[q].x, fl), __fdiv_rn(v[q].y, fl), __fdiv_rn(v[q].z, fl),
+                                               __fdiv_rn(v[q].w, fl));
+                        }
                         if (q0 + q == 0 && g32 == 0 && x_warp) {  // x, exactly (output rows are W floats apart)
                             float* dst = stage + (row / NP) * W + c32 * 4;
                             dst[0] = v[q].x;
@@ -634,7 +729,7 @@ int sm_count()
     return cached[dev];
 }
 
-template <int D, typename TE, typename TI, int MODE, int NP>
+template <int D, typename TE, typename TI, int MODE, int NP, bool MULTI>
 dlrm_status launch_tc(const FwdArgs& a, cudaStream_t stream)
 {
     constexpr int S = kTileRows / NP;
@@ -644,7 +739,7 @@ dlrm_status launch_tc(const FwdArgs& a, cudaStream_t stream)
     int smem = L.bytes + 1024;  // + alignment of the operands to 1024 bytes
     if (smem < kMinSmemPerCta) smem = kMinSmemPerCta;
     if (smem > kMaxSmem) return DLRM_ERR_UNSUPPORTED;
-    auto kern = forward_tc_kernel<D, TE, TI, MODE, NP>;
+    auto kern = forward_tc_kernel<D, TE, TI, MODE, NP, MULTI>;
     static int configured = 0;  // per instantiation
     if (!configured) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess ||
@@ -671,24 +766,32 @@ dlrm_status launch_tc(const FwdArgs& a, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
-template <int D, typename TE, typename TI, int MODE>
+template <int D, typename TE, typename TI, int MODE, bool MULTI>
 dlrm_status dispatch_np(const FwdArgs& a, cudaStream_t s)
 {
     const int N = a.T + 1;
-    if (N <= 32) return launch_tc<D, TE, TI, MODE, 32>(a, s);
-    if (N <= 64) return launch_tc<D, TE, TI, MODE, 64>(a, s);
-    return launch_tc<D, TE, TI, MODE, 128>(a, s);
+    if (N <= 32) return launch_tc<D, TE, TI, MODE, 32, MULTI>(a, s);
+    if (N <= 64) return launch_tc<D, TE, TI, MODE, 64, MULTI>(a, s);
+    return launch_tc<D, TE, TI, MODE, 128, MULTI>(a, s);
+}
+
+// Bags average more than 1.25 lookups: the multi-lookup variant.
+inline bool multi_hot(const FwdArgs& a) { return 4 * a.nnz > 5 * static_cast<int64_t>(a.T) * a.B; }
+
+template <int D, typename TE, typename TI>
+dlrm_status dispatch_fused(const FwdArgs& a, cudaStream_t s)
+{
+    return multi_hot(a) ? dispatch_np<D, TE, TI, kFused, true>(a, s) : dispatch_np<D, TE, TI, kFused, false>(a, s);
 }
 
 template <int D>
 dlrm_status dispatch_tc(int mode, const FwdArgs& a, int dtype, int index_type, cudaStream_t s)
 {
-    if (mode == kInteract) return dispatch_np<D, float, int32_t, kInteract>(a, s);
+    if (mode == kInteract) return dispatch_np<D, float, int32_t, kInteract, false>(a, s);
     if (dtype == DLRM_F32)
-        return index_type == DLRM_I32 ? dispatch_np<D, float, int32_t, kFused>(a, s)
-                                      : dispatch_np<D, float, int64_t, kFused>(a, s);
-    return index_type == DLRM_I32 ? dispatch_np<D, __nv_bfloat16, int32_t, kFused>(a, s)
-                                  : dispatch_np<D, __nv_bfloat16, int64_t, kFused>(a, s);
+        return index_type == DLRM_I32 ? dispatch_fused<D, float, int32_t>(a, s) : dispatch_fused<D, float, int64_t>(a, s);
+    return index_type == DLRM_I32 ? dispatch_fused<D, __nv_bfloat16, int32_t>(a, s)
+                                  : dispatch_fused<D, __nv_bfloat16, int64_t>(a, s);
 }
 
 }  // namespace
@@ -697,9 +800,9 @@ bool forward_tc_supported(int mode, int dim, int num_tables, int64_t batch, int6
 {
     if (!((mode == kFused || mode == kInteract) && (dim == 64 || dim == 128) && num_tables + 1 <= kTileRows))
         return false;
-    // bags average at most two lookups: the gather here keeps whole rows in
-    // flight; longer bags are pooled row by row and go to the register-pooling kernel
-    return mode == kInteract || nnz <= 2 * static_cast<int64_t>(num_tables) * batch;
+    // bags averaging more than 16 lookups are pooled faster by the register-pooling kernel,
+    // whose half-warps read two rows per instruction
+    return mode == kInteract || nnz <= 16 * static_cast<int64_t>(num_tables) * batch;
 }
 
 dlrm_status launch_forward_tc(int mode, const FwdArgs& a, int dim, int dtype, int index_type, cudaStream_t s)

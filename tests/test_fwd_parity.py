@@ -122,11 +122,12 @@ def test_identity_tables_exact_interaction(D, path):
             assert out[b, D + k] == want
 
 
-@pytest.mark.parametrize("itype,Lmax", [("i32", 4), ("i64", 4), ("i32", 2)])
-def test_bad_inputs_flag_and_zero(itype, Lmax, orc):
-    """Bags of up to 4 lookups run on the register-pooling kernel, up to 2 on the tensor-core one."""
+@pytest.mark.parametrize("itype,Lmin,Lmax", [("i32", 1, 4), ("i64", 1, 4), ("i32", 1, 2), ("i32", 0, 2)])
+def test_bad_inputs_flag_and_zero(itype, Lmin, Lmax, orc):
+    """Out-of-range indices and malformed offsets on the tensor-core kernel: its multi-lookup
+    variant (bags of 1..4 or 1..2) and its one-hot variant (bags of 0..2, mean length 1)."""
     B, T, D = 9, 3, 64
-    tabs, Vs, idx, off, dense = random_case(11, B, T, D, 20, 1, Lmax)
+    tabs, Vs, idx, off, dense = random_case(11, B, T, D, 20, Lmin, Lmax)
     idx[2] = 20        # == V: out of range
     idx[5] = -1
     idx[-1] = 1 << 30
