@@ -82,11 +82,11 @@ def algorithmic_bytes(w: gen.Workload, batch: gen.Batch) -> int:
 
 
 def sort_passes(w: gen.Workload) -> int:
-    """LSD radix passes of 8 bits over keys below the total row count."""
+    """LSD radix passes (digits of at most 9 bits) over keys below the total row count."""
     bits = 1
     while (1 << bits) <= sum(w.num_rows):
         bits += 1
-    return (bits + 7) // 8
+    return (bits + 8) // 9
 
 
 def train_bytes(w: gen.Workload, batch: gen.Batch) -> dict:

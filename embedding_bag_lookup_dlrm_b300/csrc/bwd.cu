@@ -25,8 +25,8 @@ constexpr uint32_t kSentinel = 0xFFFFFFFFu;  // key of a lookup that updates not
 constexpr int kSortThreads = 256;
 constexpr int kSortItems = 16;
 constexpr int kSortTile = kSortThreads * kSortItems;  // 4096 keys per tile
-constexpr int kRadixBits = 8;
-constexpr int kBins = 1 << kRadixBits;
+constexpr int kMaxRadixBits = 9;  // digit width of a pass: up to 9 bits
+constexpr int kMaxBins = 1 << kMaxRadixBits;
 constexpr int kChunk = 128;  // sorted lookups per segment-reduction warp
 constexpr int kSegThreads = 128;
 
@@ -36,8 +36,8 @@ struct Workspace {
     float* dP;          // B x T x D
     uint32_t* keys[2];  // nnz each, ping-pong
     uint32_t* vals[2];
-    uint32_t* counts;   // kBins x num_tiles
-    uint32_t* bin_total;  // kBins
+    uint32_t* counts;   // kMaxBins x num_tiles
+    uint32_t* bin_total;  // kMaxBins
     float* partial;     // 2 x num_chunks x D
     int64_t num_tiles, num_chunks;
 };
@@ -59,8 +59,8 @@ Workspace carve(void* base, int64_t B, int32_t T, int32_t D, int64_t nnz, size_t
         o_k[i] = take(sizeof(uint32_t) * nnz);
         o_v[i] = take(sizeof(uint32_t) * nnz);
     }
-    const size_t o_cnt = take(sizeof(uint32_t) * kBins * (w.num_tiles > 0 ? w.num_tiles : 1));
-    const size_t o_tot = take(sizeof(uint32_t) * kBins);
+    const size_t o_cnt = take(sizeof(uint32_t) * kMaxBins * (w.num_tiles > 0 ? w.num_tiles : 1));
+    const size_t o_tot = take(sizeof(uint32_t) * kMaxBins);
     const size_t o_par = take(sizeof(float) * 2 * (w.num_chunks > 0 ? w.num_chunks : 1) * D);
     if (total) *total = o;
     if (base) {
@@ -263,28 +263,33 @@ __global__ void expand_keys_kernel(const __grid_constant__ BwdArgs a, uint32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// 3. Stable LSD radix sort of (key, value) pairs by key, 8 bits per pass.
+// 3. Stable LSD radix sort of (key, value) pairs by key, up to 9 bits per pass
+//    (digits of `dbits` bits, bins = 2^dbits):
 //    hist:    digit counts per tile of 4096 pairs   -> counts[digit][tile]
 //    scan:    per digit, exclusive scan over tiles; digit totals
-//    scatter: each pair to digit base + tile offset + its stable rank among
-//             equal digits of the tile (earlier positions first)
+//    scatter: rank each pair among equal digits of its tile (earlier
+//             positions first), reorder the tile by digit in shared memory,
+//             then write each digit's run to its place: digit base + tile
+//             offset, so neighbouring threads write neighbouring positions.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(const uint32_t* __restrict__ keys, int64_t n,
-                                                                  int shift, uint32_t* __restrict__ counts,
+                                                                  int shift, int dbits, uint32_t* __restrict__ counts,
                                                                   int64_t num_tiles)
 {
-    __shared__ uint32_t h[kBins];
-    for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = 0;
+    __shared__ uint32_t h[kMaxBins];
+    const int bins = 1 << dbits;
+    const uint32_t dmask = static_cast<uint32_t>(bins - 1);
+    for (int i = threadIdx.x; i < bins; i += blockDim.x) h[i] = 0;
     __syncthreads();
     const int64_t tile = blockIdx.x;
     const int64_t t0 = tile * kSortTile;
 #pragma unroll 4
     for (int i = 0; i < kSortItems; ++i) {
         const int64_t p = t0 + i * kSortThreads + threadIdx.x;
-        if (p < n) atomicAdd(&h[(keys[p] >> shift) & (kBins - 1)], 1u);
+        if (p < n) atomicAdd(&h[(keys[p] >> shift) & dmask], 1u);
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < kBins; d += blockDim.x) counts[d * num_tiles + tile] = h[d];
+    for (int d = threadIdx.x; d < bins; d += blockDim.x) counts[d * num_tiles + tile] = h[d];
 }
 
 // One CTA per digit: in-place exclusive scan of counts[digit][0..num_tiles).
@@ -318,40 +323,65 @@ __global__ void __launch_bounds__(256) radix_scan_kernel(uint32_t* __restrict__ 
     if (threadIdx.x == 0) bin_total[blockIdx.x] = carry;
 }
 
+// Exclusive scan, in place, of v[0..kMaxBins) by the 256 threads of a block
+// (two consecutive entries per thread); returns nothing, v holds the prefixes.
+__device__ __forceinline__ void block_exclusive_scan_bins(uint32_t* v, uint32_t* wsum)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t a0 = v[2 * threadIdx.x], a1 = v[2 * threadIdx.x + 1];
+    const uint32_t pair = a0 + a1;
+    uint32_t x = pair;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, s);
+        if (lane >= s) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    const uint32_t excl = before + x - pair;
+    __syncthreads();
+    v[2 * threadIdx.x] = excl;
+    v[2 * threadIdx.x + 1] = excl + a0;
+    __syncthreads();
+}
+
+struct ScatterSmem {
+    uint32_t warp_cnt[kSortThreads / kWarp][kMaxBins];  // per warp digit counts, then their prefixes
+    uint32_t base_of[kMaxBins];                          // global position of the tile's first pair of a digit
+    uint32_t tile_start[kMaxBins];                       // position of a digit's first pair in the reordered tile
+    uint32_t wsum[kSortThreads / kWarp];
+    uint32_t key[kSortTile];
+    uint32_t val[kSortTile];
+};
+
 __global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
     const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
-    uint32_t* __restrict__ vals_out, int64_t n, int shift, const uint32_t* __restrict__ counts, int64_t num_tiles,
-    const uint32_t* __restrict__ bin_total)
+    uint32_t* __restrict__ vals_out, int64_t n, int shift, int dbits, const uint32_t* __restrict__ counts,
+    int64_t num_tiles, const uint32_t* __restrict__ bin_total)
 {
     constexpr int kWarps = kSortThreads / kWarp;
     constexpr int kPerWarp = kSortTile / kWarps;  // 512 consecutive pairs per warp
-    __shared__ uint32_t warp_cnt[kWarps][kBins];
-    __shared__ uint32_t base_of[kBins];
+    extern __shared__ __align__(16) unsigned char sort_smem[];
+    ScatterSmem& sm = *reinterpret_cast<ScatterSmem*>(sort_smem);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t tile = blockIdx.x;
+    const int bins = 1 << dbits;
+    const uint32_t dmask = static_cast<uint32_t>(bins - 1);
+    const int64_t t0 = tile * kSortTile;
+    const int tile_n = static_cast<int>(min(static_cast<int64_t>(kSortTile), n - t0));
 
-    for (int i = threadIdx.x; i < kWarps * kBins; i += blockDim.x) (&warp_cnt[0][0])[i] = 0;
-    // digit bases: exclusive scan of the digit totals (kBins values, one thread each)
-    {
-        const int d = threadIdx.x;  // kSortThreads == kBins
-        const uint32_t v = bin_total[d];
-        uint32_t x = v;
-#pragma unroll
-        for (int s = 1; s < 32; s <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, x, s);
-            if (lane >= s) x += y;
-        }
-        __shared__ uint32_t wsum[kWarps];
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        uint32_t before = 0;
-        for (int w = 0; w < warp; ++w) before += wsum[w];
-        base_of[d] = before + x - v + counts[d * num_tiles + tile];
-    }
+    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+    // digit bases: exclusive scan of the digit totals, plus this tile's offset within each digit
+    for (int d = threadIdx.x; d < kMaxBins; d += blockDim.x) sm.base_of[d] = d < bins ? bin_total[d] : 0u;
     __syncthreads();
+    block_exclusive_scan_bins(sm.base_of, sm.wsum);
+    for (int d = threadIdx.x; d < bins; d += blockDim.x) sm.base_of[d] += counts[d * num_tiles + tile];
 
+    // stable ranks: warp w ranks pairs w*512 .. w*512+511 of the tile in order, 32 at a time
     const uint32_t lt_mask = (1u << lane) - 1u;
-    const int64_t w0 = tile * kSortTile + warp * kPerWarp;
+    const int64_t w0 = t0 + warp * kPerWarp;
     uint32_t key[kPerWarp / kWarp], val[kPerWarp / kWarp], rank[kPerWarp / kWarp];
 #pragma unroll
     for (int r = 0; r < kPerWarp / kWarp; ++r) {
@@ -359,37 +389,48 @@ __global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
         const bool live = p < n;
         key[r] = live ? keys_in[p] : 0u;
         val[r] = live ? vals_in[p] : 0u;
-        const uint32_t d = (key[r] >> shift) & (kBins - 1);
+        const uint32_t d = (key[r] >> shift) & dmask;
         const uint32_t live_mask = __ballot_sync(0xffffffffu, live);
-        uint32_t peers = __match_any_sync(0xffffffffu, live ? d : 0xFFFFFFFFu) & live_mask;
-        const uint32_t before = warp_cnt[warp][d];
+        const uint32_t peers = __match_any_sync(0xffffffffu, live ? d : 0xFFFFFFFFu) & live_mask;
+        const uint32_t before = sm.warp_cnt[warp][d];
         rank[r] = before + __popc(peers & lt_mask);
         __syncwarp();
-        if (live && (peers & ~((lt_mask << 1) | 1u)) == 0) warp_cnt[warp][d] = before + __popc(peers);  // last peer
+        if (live && (peers & ~((lt_mask << 1) | 1u)) == 0) sm.warp_cnt[warp][d] = before + __popc(peers);  // last peer
         __syncwarp();
     }
     __syncthreads();
-    // exclusive prefix of the per-warp digit counts across warps (warp order = position order)
-    {
-        const int d = threadIdx.x;
+    // per digit: exclusive prefix over warps (warp order = position order) and the tile's digit count
+    for (int d = threadIdx.x; d < kMaxBins; d += blockDim.x) {
         uint32_t run = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const uint32_t c = warp_cnt[w][d];
-            warp_cnt[w][d] = run;
+            const uint32_t c = sm.warp_cnt[w][d];
+            sm.warp_cnt[w][d] = run;
             run += c;
         }
+        sm.tile_start[d] = run;
     }
     __syncthreads();
+    block_exclusive_scan_bins(sm.tile_start, sm.wsum);
+    // the tile reordered by digit (stable), in shared memory
 #pragma unroll
     for (int r = 0; r < kPerWarp / kWarp; ++r) {
         const int64_t p = w0 + r * kWarp + lane;
         if (p < n) {
-            const uint32_t d = (key[r] >> shift) & (kBins - 1);
-            const uint32_t dst = base_of[d] + warp_cnt[warp][d] + rank[r];
-            keys_out[dst] = key[r];
-            vals_out[dst] = val[r];
+            const uint32_t d = (key[r] >> shift) & dmask;
+            const uint32_t at = sm.tile_start[d] + sm.warp_cnt[warp][d] + rank[r];
+            sm.key[at] = key[r];
+            sm.val[at] = val[r];
         }
+    }
+    __syncthreads();
+    // each digit's run to its place: consecutive threads, consecutive positions
+    for (int i = threadIdx.x; i < tile_n; i += kSortThreads) {
+        const uint32_t k = sm.key[i];
+        const uint32_t d = (k >> shift) & dmask;
+        const uint32_t dst = sm.base_of[d] + (static_cast<uint32_t>(i) - sm.tile_start[d]);
+        keys_out[dst] = k;
+        vals_out[dst] = sm.val[i];
     }
 }
 
@@ -674,9 +715,12 @@ dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
 template <int D, typename TI>
 dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
 {
-    // interaction backward: a sample's g V is shared by 8 warps for wide N
+    // interaction backward (the warps per sample are chosen below)
     const int nblk = round_up(a.T + 1, 8) / 8;
-    dlrm_status st = nblk > 8 ? launch_interact_bwd<D, 8, TI>(a, w.dP, s) : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
+    // warps per sample: one per 8-row block of dV up to 4 (N <= 32), else 8; a sample's V is staged once
+    dlrm_status st = nblk > 4   ? launch_interact_bwd<D, 8, TI>(a, w.dP, s)
+                     : nblk > 2 ? launch_interact_bwd<D, 4, TI>(a, w.dP, s)
+                                : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
     if (st != DLRM_OK) return st;
     if (a.nnz == 0) return DLRM_OK;
 
@@ -685,16 +729,27 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
     expand_keys_kernel<TI><<<static_cast<unsigned>((nbags + 255) / 256 < 148 * 64 ? (nbags + 255) / 256 : 148 * 64), 256, 0, s>>>(
         a, w.keys[0], w.vals[0]);
 
-    // key bits: valid keys are < total rows, so the sentinel's low bits sort after them
+    // key bits: valid keys are < total rows, so the sentinel's low bits sort after them; the passes
+    // split them into digits of at most kMaxRadixBits bits
     int bits = 1;
     while ((int64_t{1} << bits) <= a.row_base[a.T]) ++bits;
+    const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
+    const int dbits = (bits + passes - 1) / passes;
+    static bool scatter_configured = false;
+    if (!scatter_configured) {
+        if (cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sizeof(ScatterSmem))) != cudaSuccess)
+            return DLRM_ERR_CUDA;
+        scatter_configured = true;
+    }
     int cur = 0;
-    for (int shift = 0; shift < bits; shift += kRadixBits) {
+    for (int pass = 0; pass < passes; ++pass) {
+        const int shift = pass * dbits;
         radix_hist_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, 0, s>>>(w.keys[cur], a.nnz, shift,
-                                                                                     w.counts, w.num_tiles);
-        radix_scan_kernel<<<kBins, 256, 0, s>>>(w.counts, w.num_tiles, w.bin_total);
-        radix_scatter_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, 0, s>>>(
-            w.keys[cur], w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], a.nnz, shift, w.counts, w.num_tiles,
+                                                                                     dbits, w.counts, w.num_tiles);
+        radix_scan_kernel<<<1u << dbits, 256, 0, s>>>(w.counts, w.num_tiles, w.bin_total);
+        radix_scatter_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, sizeof(ScatterSmem), s>>>(
+            w.keys[cur], w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], a.nnz, shift, dbits, w.counts, w.num_tiles,
             w.bin_total);
         cur ^= 1;
     }
