@@ -660,28 +660,52 @@ __global__ void __launch_bounds__(kSegThreads) segment_span_kernel(const __grid_
     if (key == kSentinel || keys[c1] != key) return;     // last run not cut
     const bool whole = keys[c0] == key;                   // chunk is one run
     if (whole && c0 > 0 && keys[c0 - 1] == key) return;   // run started in an earlier chunk
-    const int t = static_cast<int>(vals[c1 - 1] % static_cast<uint32_t>(a.T));
+    const uint32_t v_last = vals[c1 - 1];
+    const int t = static_cast<int>(v_last - div_by_T(v_last, a) * static_cast<uint32_t>(a.T));
 
+    // the run holds a piece of every later chunk whose first key is its key: those chunks are
+    // consecutive; find the last, 32 chunk borders at a time
+    int64_t last = chunk;
+    for (int64_t cb = chunk + 1;; cb += kWarp) {
+        const int64_t c = cb + lane;
+        const bool piece = c < num_chunks && keys[c * kChunk] == key;
+        const uint32_t m = __ballot_sync(0xffffffffu, piece);
+        const int n = m == 0xffffffffu ? kWarp : __ffs(~m) - 1;  // leading pieces
+        last = cb + n - 1;
+        if (n < kWarp) break;
+    }
+
+    // partial sums added in chunk order (the reproducible order), 8 in flight
     float4 g[C];
 #pragma unroll
     for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](int64_t slot) {
-        if (!active) return;
-        const float* src = partial + slot * D;
+    auto add = [&](const float4 (&v)[C]) {
 #pragma unroll
         for (int k = 0; k < C; ++k) {
-            const float4 v = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
-            g[k].x += v.x;
-            g[k].y += v.y;
-            g[k].z += v.z;
-            g[k].w += v.w;
+            g[k].x += v[k].x;
+            g[k].y += v[k].y;
+            g[k].z += v[k].z;
+            g[k].w += v[k].w;
         }
     };
-    add(chunk * 2 + (whole ? 0 : 1));
-    for (int64_t c = chunk + 1; c < num_chunks; ++c) {
-        add(c * 2);
-        const int64_t e = min((c + 1) * kChunk, a.nnz);
-        if (e >= a.nnz || keys[e] != key) break;
+    auto load = [&](int64_t slot, float4 (&v)[C]) {
+        const float* src = partial + slot * D;
+#pragma unroll
+        for (int k = 0; k < C; ++k) v[k] = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
+    };
+    if (active) {
+        float4 first[C];
+        load(chunk * 2 + (whole ? 0 : 1), first);
+        add(first);
+        for (int64_t c = chunk + 1; c <= last; c += 8) {
+            float4 v[8][C];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c + u <= last) load((c + u) * 2, v[u]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (c + u <= last) add(v[u]);
+        }
     }
     adagrad_row<D>(a, key, t, g, lane);
 }
