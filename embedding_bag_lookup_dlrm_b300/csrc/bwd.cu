@@ -23,8 +23,8 @@ constexpr uint32_t kSentinel = 0xFFFFFFFFu;  // key of a lookup that updates not
 
 // ---- workspace layout ------------------------------------------------------
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 16;
-constexpr int kSortTile = kSortThreads * kSortItems;  // 4096 keys per tile
+constexpr int kSortItems = 8;
+constexpr int kSortTile = kSortThreads * kSortItems;  // 2048 keys per tile
 constexpr int kMaxRadixBits = 9;  // digit width of a pass: up to 9 bits
 constexpr int kMaxBins = 1 << kMaxRadixBits;
 constexpr int kChunk = 128;  // sorted lookups per segment-reduction warp
@@ -283,11 +283,15 @@ __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(const uint32_t
     __syncthreads();
     const int64_t tile = blockIdx.x;
     const int64_t t0 = tile * kSortTile;
-#pragma unroll 4
-    for (int i = 0; i < kSortItems; ++i) {
+    uint32_t k[kSortItems];
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i) {  // every load in flight first
         const int64_t p = t0 + i * kSortThreads + threadIdx.x;
-        if (p < n) atomicAdd(&h[(keys[p] >> shift) & dmask], 1u);
+        k[i] = p < n ? keys[p] : 0u;
     }
+#pragma unroll
+    for (int i = 0; i < kSortItems; ++i)
+        if (t0 + i * kSortThreads + threadIdx.x < n) atomicAdd(&h[(k[i] >> shift) & dmask], 1u);
     __syncthreads();
     for (int d = threadIdx.x; d < bins; d += blockDim.x) counts[d * num_tiles + tile] = h[d];
 }
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
     int64_t num_tiles, const uint32_t* __restrict__ bin_total)
 {
     constexpr int kWarps = kSortThreads / kWarp;
-    constexpr int kPerWarp = kSortTile / kWarps;  // 512 consecutive pairs per warp
+    constexpr int kPerWarp = kSortTile / kWarps;  // consecutive pairs per warp
     extern __shared__ __align__(16) unsigned char sort_smem[];
     ScatterSmem& sm = *reinterpret_cast<ScatterSmem*>(sort_smem);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -372,23 +376,37 @@ __global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
     const int64_t t0 = tile * kSortTile;
     const int tile_n = static_cast<int>(min(static_cast<int64_t>(kSortTile), n - t0));
 
-    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
-    // digit bases: exclusive scan of the digit totals, plus this tile's offset within each digit
-    for (int d = threadIdx.x; d < kMaxBins; d += blockDim.x) sm.base_of[d] = d < bins ? bin_total[d] : 0u;
-    __syncthreads();
-    block_exclusive_scan_bins(sm.base_of, sm.wsum);
-    for (int d = threadIdx.x; d < bins; d += blockDim.x) sm.base_of[d] += counts[d * num_tiles + tile];
-
-    // stable ranks: warp w ranks pairs w*512 .. w*512+511 of the tile in order, 32 at a time
-    const uint32_t lt_mask = (1u << lane) - 1u;
+    // every global load of the thread first: its pairs, two digit totals, two tile offsets
     const int64_t w0 = t0 + warp * kPerWarp;
     uint32_t key[kPerWarp / kWarp], val[kPerWarp / kWarp], rank[kPerWarp / kWarp];
 #pragma unroll
     for (int r = 0; r < kPerWarp / kWarp; ++r) {
         const int64_t p = w0 + r * kWarp + lane;
+        key[r] = p < n ? keys_in[p] : 0u;
+        val[r] = p < n ? vals_in[p] : 0u;
+    }
+    uint32_t tot[2], off[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int d = 2 * threadIdx.x + j;
+        tot[j] = d < bins ? bin_total[d] : 0u;
+        off[j] = d < bins ? counts[d * num_tiles + tile] : 0u;
+    }
+    for (int i = threadIdx.x; i < kWarps * kMaxBins; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+    // digit bases: exclusive scan of the digit totals, plus this tile's offset within each digit
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sm.base_of[2 * threadIdx.x + j] = tot[j];
+    __syncthreads();
+    block_exclusive_scan_bins(sm.base_of, sm.wsum);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sm.base_of[2 * threadIdx.x + j] += off[j];
+
+    // stable ranks: warp w ranks pairs w*kPerWarp .. of the tile in order, 32 at a time
+    const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < kPerWarp / kWarp; ++r) {
+        const int64_t p = w0 + r * kWarp + lane;
         const bool live = p < n;
-        key[r] = live ? keys_in[p] : 0u;
-        val[r] = live ? vals_in[p] : 0u;
         const uint32_t d = (key[r] >> shift) & dmask;
         const uint32_t live_mask = __ballot_sync(0xffffffffu, live);
         const uint32_t peers = __match_any_sync(0xffffffffu, live ? d : 0xFFFFFFFFu) & live_mask;
