@@ -86,34 +86,41 @@ __device__ __forceinline__ int64_t ld_index(const void* p, int64_t i)
 // ---------------------------------------------------------------------------
 // 1. Interaction backward.  One group of G warps per sample.  V (x, then the
 // pooled rows) arrives by two bulk copies; the symmetric upstream matrix g
-// (zero diagonal) is built in shared memory from the triangle.  Each lane owns
-// 16-byte column chunks of V and accumulates an 8-row block of dV = g V.
+// (zero diagonal) is built in shared memory from the triangle, each entry
+// stored twice as a float2 so that one broadcast 16-byte load feeds two packed
+// fp32 FMAs (fma.rn.f32x2: two independent fused multiply-adds, each rounded
+// once, as fmaf); where that copy of g does not fit in shared memory, g is
+// stored once and the FMAs are scalar.  Each lane owns 16-byte column chunks
+// of V and accumulates an 8-row block of dV = g V, summing over j in
+// increasing order.
 // ---------------------------------------------------------------------------
 struct BwdLayout {
-    int N, NP, K;  // NP = N rounded up to 8 (rows of g)
-    int off_V, off_g, off_tri, bytes;
+    int N, NP, K, W;  // NP = N rounded up to 8 (rows of g); W = D + K (upstream row)
+    int off_V, off_g, off_go, bytes;
 };
 
-__host__ __device__ inline BwdLayout make_bwd_layout(int T, int D)
+// pair: g stored as float2 (g, g) per entry for the packed FMAs, else as float
+__host__ __device__ inline BwdLayout make_bwd_layout(int T, int D, bool pair)
 {
     BwdLayout l;
     l.N = T + 1;
     l.NP = round_up(l.N, 8);
     l.K = l.N * (l.N - 1) / 2;
+    l.W = D + l.K;
     int o = 16;  // mbarrier
     l.off_V = o;
     o += 4 * l.N * D;
     l.off_g = o;
-    o += 4 * l.NP * l.NP;
-    l.off_tri = o;
-    o += 4 * l.K;
+    o += (pair ? 8 : 4) * l.NP * l.NP;
+    l.off_go = o;
+    o += 4 * l.W;
     l.bytes = round_up(o, 128);
     return l;
 }
 
 // In mean mode dP[b][t] is stored already divided by the bag length L (the
 // scale every lookup of the bag applies), so the per-row sums are plain sums.
-template <int D, int G, typename TI>
+template <int D, int G, typename TI, bool PAIR>
 __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant__ BwdArgs a, float* __restrict__ dP,
                                                            int groups_per_cta)
 {
@@ -123,7 +130,7 @@ __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant
     constexpr int LPR = CPR < kWarp ? CPR : kWarp;   // lanes per row
     constexpr int CPL = CPR / LPR;                   // chunks per lane
     constexpr int RPI = kWarp / LPR;                 // row blocks worked on side by side
-    const BwdLayout l = make_bwd_layout(a.T, D);
+    const BwdLayout l = make_bwd_layout(a.T, D, PAIR);
     const int group = threadIdx.x / GT;
     const int gl = threadIdx.x % GT;
     const int lane = gl % kWarp;
@@ -135,9 +142,8 @@ __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant
     uint64_t* bar = reinterpret_cast<uint64_t*>(base);
     float* V = reinterpret_cast<float*>(base + l.off_V);
     float* gm = reinterpret_cast<float*>(base + l.off_g);
-    float* tri = reinterpret_cast<float*>(base + l.off_tri);
-    const int T = a.T, N = l.N, NP = l.NP, K = l.K;
-    const int W = D + K;
+    float* gos = reinterpret_cast<float*>(base + l.off_go);  // the sample's upstream row: d(out)[0..W)
+    const int T = a.T, N = l.N, NP = l.NP, W = l.W;
 
     if (gl == 0) {
         mbar_init(bar, 1);
@@ -151,44 +157,83 @@ __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant
         bulk_g2s(V + D, a.pooled + b * T * D, pb, bar);
     }
     const float* go = a.grad_out + b * W;
-    for (int k = gl; k < K; k += GT) tri[k] = go[D + k];
+    for (int k = gl; k < W; k += GT) gos[k] = go[k];
     if (G == 1) __syncwarp(); else __syncthreads();
-    for (int e = gl; e < NP * NP; e += GT) {
-        const int i = e / NP, j = e - (e / NP) * NP;
-        float v = 0.0f;
-        if (i < N && j < N && i != j) v = tri[i < j ? tri_index(i, j, N) : tri_index(j, i, N)];
-        gm[e] = v;
+    {
+        // entries e = gl, gl + GT, ... of the NP x NP matrix, (i, j) stepped without a division per entry
+        const float* tri = gos + D;
+        const int di = GT / NP, dj = GT - di * NP;
+        int i = gl / NP, j = gl - (gl / NP) * NP;
+        for (int e = gl; e < NP * NP; e += GT) {
+            float v = 0.0f;
+            if (i < N && j < N && i != j) v = tri[i < j ? tri_index(i, j, N) : tri_index(j, i, N)];
+            if constexpr (PAIR)
+                reinterpret_cast<float2*>(gm)[e] = make_float2(v, v);
+            else
+                gm[e] = v;
+            i += di;
+            j += dj;
+            if (j >= NP) {
+                j -= NP;
+                ++i;
+            }
+        }
     }
     const bool landed = mbar_wait_bounded(bar, 0);
     const bool failed = (G == 1) ? (__any_sync(0xffffffffu, !landed) != 0) : (__syncthreads_or(!landed) != 0);
     if (failed) {
-        if (gl == 0) flag_status(a.status, DLRM_ERR_TIMEOUT);
+        if (gl == 0) {
+            flag_status(a.status, DLRM_ERR_TIMEOUT);
+            (void)mbar_wait_bounded(bar, 0);  // the copy still in flight ends before the group leaves
+        }
         return;
     }
     if (G == 1) __syncwarp();
 
-    const int h = lane / LPR;            // row-block lane set
+    const int h = lane / LPR;  // row-block lane set
     const int c0 = lane % LPR;
     const int nblk = NP / 8;
     for (int ib = wig * RPI + h; ib < nblk; ib += G * RPI) {
         const int i0 = ib * 8;
 #pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-            const int col = (c0 + k * LPR) * 4;
+        for (int c = 0; c < CPL; ++c) {
+            const int col = (c0 + c * LPR) * 4;
             float4 acc[8];
+            if constexpr (PAIR) {
+                float2 lo[8], hi[8];  // row i0 + r: columns col, col+1 and col+2, col+3
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < N; ++j) {
-                const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
-                const float4 g0 = *reinterpret_cast<const float4*>(gm + j * NP + i0);
-                const float4 g1 = *reinterpret_cast<const float4*>(gm + j * NP + i0 + 4);
-                const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                for (int r = 0; r < 8; ++r) lo[r] = hi[r] = make_float2(0.f, 0.f);
+                for (int j = 0; j < N; ++j) {
+                    const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
+                    const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
+                    const float4* gj = reinterpret_cast<const float4*>(gm + 2 * (j * NP + i0));
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    acc[r].x = fmaf(gg[r], v.x, acc[r].x);
-                    acc[r].y = fmaf(gg[r], v.y, acc[r].y);
-                    acc[r].z = fmaf(gg[r], v.z, acc[r].z);
-                    acc[r].w = fmaf(gg[r], v.w, acc[r].w);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 g2 = gj[q];  // (g, g) of rows i0 + 2q and i0 + 2q + 1
+                        const float2 ga = make_float2(g2.x, g2.y), gb = make_float2(g2.z, g2.w);
+                        lo[2 * q] = __ffma2_rn(ga, v01, lo[2 * q]);
+                        hi[2 * q] = __ffma2_rn(ga, v23, hi[2 * q]);
+                        lo[2 * q + 1] = __ffma2_rn(gb, v01, lo[2 * q + 1]);
+                        hi[2 * q + 1] = __ffma2_rn(gb, v23, hi[2 * q + 1]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[r] = make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y);
+            } else {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < N; ++j) {
+                    const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
+                    const float4 g0 = *reinterpret_cast<const float4*>(gm + j * NP + i0);
+                    const float4 g1 = *reinterpret_cast<const float4*>(gm + j * NP + i0 + 4);
+                    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        acc[r].x = fmaf(gg[r], v.x, acc[r].x);
+                        acc[r].y = fmaf(gg[r], v.y, acc[r].y);
+                        acc[r].z = fmaf(gg[r], v.z, acc[r].z);
+                        acc[r].w = fmaf(gg[r], v.w, acc[r].w);
+                    }
                 }
             }
 #pragma unroll
@@ -197,10 +242,10 @@ __global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant
                 if (i >= N) break;
                 if (i == 0) {
                     float4 u;
-                    u.x = go[col] + acc[0].x;
-                    u.y = go[col + 1] + acc[0].y;
-                    u.z = go[col + 2] + acc[0].z;
-                    u.w = go[col + 3] + acc[0].w;
+                    u.x = gos[col] + acc[0].x;
+                    u.y = gos[col + 1] + acc[0].y;
+                    u.z = gos[col + 2] + acc[0].z;
+                    u.w = gos[col + 3] + acc[0].w;
                     *reinterpret_cast<float4*>(a.grad_dense + b * D + col) = u;
                 } else {
                     float4 u = acc[r];
@@ -231,33 +276,55 @@ __global__ void fill_u32_kernel(uint32_t* p, int64_t n, uint32_t v)
         p[i] = v;
 }
 
+// Each warp takes 32 consecutive bags (table-major order, so the lookups of
+// those bags are one contiguous range of positions) and walks the range with
+// consecutive lanes on consecutive positions.  A lane finds the bag of its
+// position p among the warp's 32 as the number of bags that end at or before
+// p (bag ends are non-decreasing), by a 5-step search over the lanes' ends.
 template <typename TI>
-__global__ void expand_keys_kernel(const __grid_constant__ BwdArgs a, uint32_t* __restrict__ keys,
-                                   uint32_t* __restrict__ vals)
+__global__ void __launch_bounds__(256) expand_keys_kernel(const __grid_constant__ BwdArgs a,
+                                                          uint32_t* __restrict__ keys, uint32_t* __restrict__ vals)
 {
     const int64_t nbags = static_cast<int64_t>(a.T) * a.B;
+    const int lane = threadIdx.x & 31;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (ld_index<TI>(a.offsets, 0) != 0 || ld_index<TI>(a.offsets, nbags) != a.nnz)
             flag_status(a.status, DLRM_ERR_BAD_OFFSETS);
     }
-    for (int64_t bag = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; bag < nbags;
-         bag += int64_t{gridDim.x} * blockDim.x) {
-        const int t = static_cast<int>(bag / a.B);
-        const int64_t b = bag - int64_t{t} * a.B;
-        const int64_t s0 = ld_index<TI>(a.offsets, bag), s1 = ld_index<TI>(a.offsets, bag + 1);
-        if (s0 < 0 || s1 < s0 || s1 > a.nnz) {
-            flag_status(a.status, DLRM_ERR_BAD_OFFSETS);
-            continue;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / kWarp);
+    for (int64_t bag0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / kWarp) + threadIdx.x / kWarp) * kWarp;
+         bag0 < nbags; bag0 += warps * kWarp) {
+        const int64_t bag = bag0 + lane;
+        const bool live = bag < nbags;
+        const int64_t s0 = live ? ld_index<TI>(a.offsets, bag) : 0;
+        const int64_t s1 = live ? ld_index<TI>(a.offsets, bag + 1) : 0;
+        if (__any_sync(0xffffffffu, live && (s0 < 0 || s1 < s0 || s1 > a.nnz))) {
+            if (lane == 0) flag_status(a.status, DLRM_ERR_BAD_OFFSETS);
+            continue;  // the warp's positions keep the sentinel key
         }
-        const uint32_t v = static_cast<uint32_t>(b * a.T + t);
-        for (int64_t p = s0; p < s1; ++p) {
-            const int64_t r = ld_index<TI>(a.indices, p);
-            if (r < 0 || r >= a.num_rows[t]) {
-                flag_status(a.status, DLRM_ERR_INDEX_OOB);
-                continue;
+        const int last = static_cast<int>(min(static_cast<int64_t>(kWarp - 1), nbags - 1 - bag0));
+        const int64_t begin = __shfl_sync(0xffffffffu, s0, 0);
+        const int64_t end = __shfl_sync(0xffffffffu, s1, last);
+        const int64_t e = live ? s1 : INT64_MAX;  // bag ends; lanes past the last bag end never
+        const int t = live ? static_cast<int>(bag / a.B) : 0;
+        const uint32_t v = live ? static_cast<uint32_t>((bag - int64_t{t} * a.B) * a.T + t) : 0u;
+        const int64_t rb = a.row_base[t], nr = a.num_rows[t];
+        for (int64_t p = begin + lane; __any_sync(0xffffffffu, p < end); p += kWarp) {
+            int at = 0;  // bags of this warp that end at or before p
+#pragma unroll
+            for (int step = 16; step >= 1; step >>= 1)
+                if (__shfl_sync(0xffffffffu, e, at + step - 1) <= p) at += step;
+            const uint32_t pv = __shfl_sync(0xffffffffu, v, at);
+            const int64_t prb = __shfl_sync(0xffffffffu, rb, at), pnr = __shfl_sync(0xffffffffu, nr, at);
+            if (p < end) {
+                const int64_t r = ld_index<TI>(a.indices, p);
+                if (r < 0 || r >= pnr) {
+                    flag_status(a.status, DLRM_ERR_INDEX_OOB);
+                } else {
+                    keys[p] = static_cast<uint32_t>(prb + r);
+                    vals[p] = pv;
+                }
             }
-            keys[p] = static_cast<uint32_t>(a.row_base[t] + r);
-            vals[p] = v;
         }
     }
 }
@@ -265,7 +332,7 @@ __global__ void expand_keys_kernel(const __grid_constant__ BwdArgs a, uint32_t* 
 // ---------------------------------------------------------------------------
 // 3. Stable LSD radix sort of (key, value) pairs by key, up to 9 bits per pass
 //    (digits of `dbits` bits, bins = 2^dbits):
-//    hist:    digit counts per tile of 4096 pairs   -> counts[digit][tile]
+//    hist:    digit counts per tile of 2048 pairs   -> counts[digit][tile]
 //    scan:    per digit, exclusive scan over tiles; digit totals
 //    scatter: rank each pair among equal digits of its tile (earlier
 //             positions first), reorder the tile by digit in shared memory,
@@ -733,10 +800,10 @@ __global__ void __launch_bounds__(kSegThreads) segment_span_kernel(const __grid_
 // ---------------------------------------------------------------------------
 constexpr int kMaxSmem = 227 * 1024;
 
-template <int D, int G, typename TI>
-dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
+template <int D, int G, typename TI, bool PAIR>
+dlrm_status launch_interact_bwd_as(const BwdArgs& a, float* dP, cudaStream_t s)
 {
-    const BwdLayout l = make_bwd_layout(a.T, D);
+    const BwdLayout l = make_bwd_layout(a.T, D, PAIR);
     int groups = 1;
     if (G == 1) {
         groups = kMaxSmem / l.bytes;
@@ -746,12 +813,20 @@ dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
         return DLRM_ERR_UNSUPPORTED;
     }
     const size_t smem = static_cast<size_t>(groups) * l.bytes;
-    auto kern = interact_bwd_kernel<D, G, TI>;
+    auto kern = interact_bwd_kernel<D, G, TI, PAIR>;
     if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
         return DLRM_ERR_CUDA;
     const int64_t blocks = (a.B + groups - 1) / groups;
     kern<<<static_cast<unsigned>(blocks), groups * G * kWarp, smem, s>>>(a, dP, groups);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
+}
+
+// g as float2 pairs for the packed FMAs when that layout fits in shared memory, else as floats
+template <int D, int G, typename TI>
+dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
+{
+    return make_bwd_layout(a.T, D, true).bytes <= kMaxSmem ? launch_interact_bwd_as<D, G, TI, true>(a, dP, s)
+                                                           : launch_interact_bwd_as<D, G, TI, false>(a, dP, s);
 }
 
 template <int D, typename TI>
@@ -768,7 +843,8 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
 
     const int64_t nbags = int64_t{a.T} * a.B;
     fill_u32_kernel<<<148 * 8, 256, 0, s>>>(w.keys[0], a.nnz, kSentinel);
-    expand_keys_kernel<TI><<<static_cast<unsigned>((nbags + 255) / 256 < 148 * 64 ? (nbags + 255) / 256 : 148 * 64), 256, 0, s>>>(
+    const int64_t expand_blocks = (nbags + 255) / 256;  // a warp per 32 bags
+    expand_keys_kernel<TI><<<static_cast<unsigned>(expand_blocks < 148 * 64 ? expand_blocks : 148 * 64), 256, 0, s>>>(
         a, w.keys[0], w.vals[0]);
 
     // key bits: valid keys are < total rows, so the sentinel's low bits sort after them; the passes

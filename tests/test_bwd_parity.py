@@ -81,6 +81,8 @@ CASES = [
     (16, 3, "mean", "i32", 1, 3, 1000, 7),
     (256, 2, "sum", "i64", 1, 1, 33, 1000),
     (32, 100, "sum", "i32", 1, 2, 21, 100),
+    # N = 113 at D = 256: g stored once (the paired copy would not fit), scalar FMAs
+    (256, 112, "mean", "i32", 0, 2, 9, 50),
 ]
 
 
@@ -139,6 +141,23 @@ def test_bwd_flags_bad_index(orc):
     dl.dlrm_sparse_bwd_adagrad(dt, acc, di, do, dx, ps, g, 0.01, 1e-8, status=status)
     torch.cuda.synchronize()
     assert status.item() & dl.DLRM_ERR_INDEX_OOB
+
+
+def test_bwd_flags_bad_offsets(orc):
+    """Offsets that go backwards: the backward flags them and touches no memory out of range."""
+    B, T, D, V = 50, 3, 64, 30
+    tabs, Vs, idx, off, dense = random_case(42, B, T, D, V, 1, 3, value_scale=0.05)
+    off = off.copy()
+    off[5] = off[6] + 2  # bag 4 ends after bag 5 does
+    dt = dev_tables(tabs, "f32")
+    acc = [torch.full((v,), 0.1, device="cuda") for v in Vs]
+    ps = torch.zeros((B, T, D), device="cuda")
+    di, do, dx = dev_index(idx, "i32"), dev_index(off, "i32"), torch.from_numpy(dense).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = torch.randn((B, D + 6), device="cuda")
+    dl.dlrm_sparse_bwd_adagrad(dt, acc, di, do, dx, ps, g, 0.01, 1e-8, status=status)
+    torch.cuda.synchronize()
+    assert status.item() & dl.DLRM_ERR_BAD_OFFSETS
 
 
 def test_workload_training_step(orc):
