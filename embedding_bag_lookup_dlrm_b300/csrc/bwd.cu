@@ -552,17 +552,17 @@ __device__ __forceinline__ void adagrad_row(const BwdArgs& a, uint32_t key, int 
     const int64_t r = static_cast<int64_t>(key) - a.row_base[t];
     float* acc = a.accum[t] + r;
     const float A = *acc + ss / static_cast<float>(D);
-    const float den = sqrtf(A) + a.eps;
+    const float step = a.lr / (sqrtf(A) + a.eps);  // one division per row
     if (active) {
         float* w = a.tables[t] + r * D;
 #pragma unroll
         for (int k = 0; k < C; ++k) {
             const int col = (lane + k * kWarp) * 4;
             float4 v = *reinterpret_cast<float4*>(w + col);
-            v.x -= a.lr * g[k].x / den;
-            v.y -= a.lr * g[k].y / den;
-            v.z -= a.lr * g[k].z / den;
-            v.w -= a.lr * g[k].w / den;
+            v.x = fmaf(-step, g[k].x, v.x);
+            v.y = fmaf(-step, g[k].y, v.y);
+            v.z = fmaf(-step, g[k].z, v.z);
+            v.w = fmaf(-step, g[k].w, v.w);
             *reinterpret_cast<float4*>(w + col) = v;
         }
     }
@@ -596,16 +596,16 @@ __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, in
     for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
     const int64_t r = static_cast<int64_t>(key) - a.row_base[t];
     const float A = acc_old + ss / static_cast<float>(D);
-    const float den = sqrtf(A) + a.eps;
+    const float step = a.lr / (sqrtf(A) + a.eps);  // one division per row
     if (active) {
         float* wr = a.tables[t] + r * D;
 #pragma unroll
         for (int k = 0; k < C; ++k) {
             float4 v = w[k];
-            v.x -= a.lr * g[k].x / den;
-            v.y -= a.lr * g[k].y / den;
-            v.z -= a.lr * g[k].z / den;
-            v.w -= a.lr * g[k].w / den;
+            v.x = fmaf(-step, g[k].x, v.x);
+            v.y = fmaf(-step, g[k].y, v.y);
+            v.z = fmaf(-step, g[k].z, v.z);
+            v.w = fmaf(-step, g[k].w, v.w);
             *reinterpret_cast<float4*>(wr + (lane + k * kWarp) * 4) = v;
         }
     }
