@@ -617,14 +617,14 @@ __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, in
 // starts in the group (each row is updated once per call, so reading it early
 // is safe), then walks the group in order.
 template <int D>
-__global__ void __launch_bounds__(kSegThreads, 4) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
+__global__ void __launch_bounds__(kSegThreads, 8) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
                                                                        const uint32_t* __restrict__ keys,
                                                                        const uint32_t* __restrict__ vals,
                                                                        const float* __restrict__ dP,
                                                                        float* __restrict__ partial, int64_t num_chunks)
 {
     constexpr int C = Lanes<D>::kChunks;
-    constexpr int U = 8;  // lookups per group
+    constexpr int U = 2;  // lookups per group
     const int lane = threadIdx.x & 31;
     const int64_t chunk = blockIdx.x * int64_t{blockDim.x / kWarp} + (threadIdx.x >> 5);
     if (chunk >= num_chunks) return;
