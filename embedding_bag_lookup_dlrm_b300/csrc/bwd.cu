@@ -363,33 +363,48 @@ __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(const uint32_t
     for (int d = threadIdx.x; d < bins; d += blockDim.x) counts[d * num_tiles + tile] = h[d];
 }
 
-// One CTA per digit: in-place exclusive scan of counts[digit][0..num_tiles).
+// One CTA per digit: in-place exclusive scan of counts[digit][0..num_tiles),
+// each thread taking 8 consecutive tiles per step (2048 tiles a step).
 __global__ void __launch_bounds__(256) radix_scan_kernel(uint32_t* __restrict__ counts, int64_t num_tiles,
                                                          uint32_t* __restrict__ bin_total)
 {
+    constexpr int IT = 8;
     __shared__ uint32_t warp_sum[8];
-    __shared__ uint32_t carry;
     uint32_t* row = counts + blockIdx.x * num_tiles;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int64_t base = 0; base < num_tiles; base += 256) {
-        const int64_t i = base + threadIdx.x;
-        const uint32_t v = i < num_tiles ? row[i] : 0u;
-        uint32_t x = v;
+    uint32_t carry = 0;  // the same in every thread
+    for (int64_t base = 0; base < num_tiles; base += 256 * IT) {
+        const int64_t i0 = base + static_cast<int64_t>(threadIdx.x) * IT;
+        uint32_t v[IT];
+        uint32_t own = 0;
 #pragma unroll
-        for (int s = 1; s < 32; s <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, x, s);
-            if (lane >= s) x += y;
+        for (int j = 0; j < IT; ++j) {
+            v[j] = i0 + j < num_tiles ? row[i0 + j] : 0u;
+            own += v[j];
+        }
+        uint32_t x = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
         }
         if (lane == 31) warp_sum[warp] = x;
         __syncthreads();
-        uint32_t before = carry;
-        for (int w = 0; w < warp; ++w) before += warp_sum[w];
-        if (i < num_tiles) row[i] = before + x - v;
-        __syncthreads();
-        if (threadIdx.x == 255) carry = before + x;
-        __syncthreads();
+        uint32_t before = carry, step = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t ws = warp_sum[w];
+            if (w < warp) before += ws;
+            step += ws;
+        }
+        uint32_t run = before + x - own;  // exclusive prefix of this thread's first tile
+#pragma unroll
+        for (int j = 0; j < IT; ++j) {
+            if (i0 + j < num_tiles) row[i0 + j] = run;
+            run += v[j];
+        }
+        carry += step;
+        __syncthreads();  // warp_sum is rewritten by the next step
     }
     if (threadIdx.x == 0) bin_total[blockIdx.x] = carry;
 }
@@ -427,7 +442,7 @@ struct ScatterSmem {
     uint32_t val[kSortTile];
 };
 
-__global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(
+__global__ void __launch_bounds__(kSortThreads, 4) radix_scatter_kernel(
     const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, int64_t n, int shift, int dbits, const uint32_t* __restrict__ counts,
     int64_t num_tiles, const uint32_t* __restrict__ bin_total)
