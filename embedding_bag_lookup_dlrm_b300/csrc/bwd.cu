@@ -121,7 +121,7 @@ __host__ __device__ inline BwdLayout make_bwd_layout(int T, int D, bool pair)
 // In mean mode dP[b][t] is stored already divided by the bag length L (the
 // scale every lookup of the bag applies), so the per-row sums are plain sums.
 template <int D, int G, typename TI, bool PAIR>
-__global__ void __launch_bounds__(256) interact_bwd_kernel(const __grid_constant__ BwdArgs a, float* __restrict__ dP,
+__global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) interact_bwd_kernel(const __grid_constant__ BwdArgs a, float* __restrict__ dP,
                                                            int groups_per_cta)
 {
     extern __shared__ __align__(128) unsigned char smem[];
