@@ -86,7 +86,7 @@ __device__ void pool_bag_warp(const TE* __restrict__ table, int64_t V_t, const v
     constexpr int LPR = CPR < kWarp ? CPR : kWarp;  // lanes per row
     constexpr int CPL = CPR / LPR;               // chunks per lane
     constexpr int RPI = kWarp / LPR;             // rows per load instruction
-    constexpr int U0 = (kWarp / RPI) < 8 ? (kWarp / RPI) : 8;
+    constexpr int U0 = (kWarp / RPI) < 16 ? (kWarp / RPI) : 16;
     constexpr int U = (U0 / CPL) > 0 ? (U0 / CPL) : 1;  // load instructions in flight
     constexpr int STEP = RPI * U;                // lookups per step (divides 32)
     static_assert(kWarp % STEP == 0, "step must divide the warp");
