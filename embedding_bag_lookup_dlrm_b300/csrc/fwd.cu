@@ -403,6 +403,10 @@ inline bool wide_interaction(int T)
     return NB * (NB + 1) / 2 > 64;
 }
 
+// Bags of 8 or more lookups on average: two warps pool a sample's bags, so a
+// sample's shared memory keeps twice the row loads in flight.
+inline bool long_bags(const FwdArgs& a) { return a.nnz >= 8 * static_cast<int64_t>(a.T) * a.B; }
+
 template <int D, typename TE, typename TI>
 dlrm_status dispatch_mode(int mode, const FwdArgs& a, cudaStream_t s)
 {
@@ -410,7 +414,8 @@ dlrm_status dispatch_mode(int mode, const FwdArgs& a, cudaStream_t s)
     switch (mode) {
         case kEmbbag: return launch_one<D, TE, TI, kEmbbag, 1>(a, s);
         case kFused:
-            return wide ? launch_one<D, TE, TI, kFused, 8>(a, s) : launch_one<D, TE, TI, kFused, 1>(a, s);
+            if (wide) return launch_one<D, TE, TI, kFused, 8>(a, s);
+            return long_bags(a) ? launch_one<D, TE, TI, kFused, 2>(a, s) : launch_one<D, TE, TI, kFused, 1>(a, s);
         default: return DLRM_ERR_UNSUPPORTED;
     }
 }

@@ -36,6 +36,8 @@ CASES = [
     (128, 100, "f32", "mean", "i32", 0, 2, 7),
     (64, 63, "f32", "sum", "i32", 1, 1, 13),
     (128, 31, "f32", "sum", "i32", 1, 1, 9),
+    # long fp32 bags (mean 25): the FFMA kernel, two warps per sample
+    (128, 26, "f32", "sum", "i64", 10, 40, 21),
 ]
 
 
