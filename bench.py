@@ -116,14 +116,13 @@ def peaks():
 
 
 FORWARD_SOURCES = ("api.cu", "common.cuh", "fwd.cu", "fwd_tc.cu", "internal.h", "tc.cuh")
+BACKWARD_SOURCES = ("api.cu", "bwd.cu", "common.cuh", "internal.h")
 
 
 def traffic_sources(workload: int):
-    """Source files of the kernels whose DRAM traffic a workload's line reports."""
-    csrc = os.path.join(ROOT, "embedding_bag_lookup_dlrm_b300", "csrc")
-    if workload == 5:
-        return sorted(os.listdir(csrc))
-    return list(FORWARD_SOURCES)
+    """Source files of the kernels whose DRAM traffic a workload's line reports: the forward's, or for
+    the training workload the backward's (its line reports the backward kernels)."""
+    return list(BACKWARD_SOURCES if workload == 5 else FORWARD_SOURCES)
 
 
 def traffic_for(workload: int):
