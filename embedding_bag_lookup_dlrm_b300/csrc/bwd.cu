@@ -632,7 +632,7 @@ __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, in
 // starts in the group (each row is updated once per call, so reading it early
 // is safe), then walks the group in order.
 template <int D>
-__global__ void __launch_bounds__(kSegThreads, 8) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
+__global__ void __launch_bounds__(kSegThreads, D >= 256 ? 4 : 8) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
                                                                        const uint32_t* __restrict__ keys,
                                                                        const uint32_t* __restrict__ vals,
                                                                        const float* __restrict__ dP,
