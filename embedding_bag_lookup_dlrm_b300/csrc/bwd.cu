@@ -13,6 +13,8 @@
 // added in chunk order), so two calls on the same inputs give the same bits.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -844,22 +846,53 @@ dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
                                                            : launch_interact_bwd_as<D, G, TI, false>(a, dP, s);
 }
 
-template <int D, typename TI>
-dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
-{
-    // interaction backward (the warps per sample are chosen below)
-    const int nblk = round_up(a.T + 1, 8) / 8;
-    // warps per sample: one per 8-row block of dV up to 4 (N <= 32), else 8; a sample's V is staged once
-    dlrm_status st = nblk > 4   ? launch_interact_bwd<D, 8, TI>(a, w.dP, s)
-                     : nblk > 2 ? launch_interact_bwd<D, 4, TI>(a, w.dP, s)
-                                : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
-    if (st != DLRM_OK) return st;
-    if (a.nnz == 0) return DLRM_OK;
+// The lookup keys are built and sorted on a second stream of the device while
+// the interaction backward runs on the caller's stream: the two read the same
+// inputs and write disjoint parts of the workspace, and only the per-row sums
+// need both.  Fork and join are events, so the pattern also holds while the
+// caller's stream is being captured into a CUDA graph.  The side stream runs
+// at the device's highest priority so that the short, dependent sort kernels
+// get SMs as soon as the interaction backward frees them.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+std::mutex g_side_mutex;  // held while a call enqueues its fork and join (the events are per device)
+SideStream g_side[64];
 
+// The device's side stream, created on first use; nullptr if it cannot be made (the sort then runs on the
+// caller's stream).  Called with g_side_mutex held.
+SideStream* side_stream()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream& sd = g_side[dev];
+    if (!sd.tried) {
+        sd.tried = true;
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&sd.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+            if (sd.join) cudaEventDestroy(sd.join);
+            if (sd.fork) cudaEventDestroy(sd.fork);
+            if (sd.stream) cudaStreamDestroy(sd.stream);
+            sd = SideStream{nullptr, nullptr, nullptr, true};
+            cudaGetLastError();  // clear the failure: the call goes on on one stream
+        }
+    }
+    return sd.stream ? &sd : nullptr;
+}
+
+// Keys, then the stable radix sort, on stream ks; returns the ping-pong buffer holding the sorted pairs.
+template <typename TI>
+dlrm_status sort_keys(const BwdArgs& a, const Workspace& w, cudaStream_t ks, int* sorted)
+{
     const int64_t nbags = int64_t{a.T} * a.B;
-    fill_u32_kernel<<<148 * 8, 256, 0, s>>>(w.keys[0], a.nnz, kSentinel);
+    fill_u32_kernel<<<148 * 8, 256, 0, ks>>>(w.keys[0], a.nnz, kSentinel);
     const int64_t expand_blocks = (nbags + 255) / 256;  // a warp per 32 bags
-    expand_keys_kernel<TI><<<static_cast<unsigned>(expand_blocks < 148 * 64 ? expand_blocks : 148 * 64), 256, 0, s>>>(
+    expand_keys_kernel<TI><<<static_cast<unsigned>(expand_blocks < 148 * 64 ? expand_blocks : 148 * 64), 256, 0, ks>>>(
         a, w.keys[0], w.vals[0]);
 
     // key bits: valid keys are < total rows, so the sentinel's low bits sort after them; the passes
@@ -878,14 +911,44 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
     int cur = 0;
     for (int pass = 0; pass < passes; ++pass) {
         const int shift = pass * dbits;
-        radix_hist_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, 0, s>>>(w.keys[cur], a.nnz, shift,
-                                                                                     dbits, w.counts, w.num_tiles);
-        radix_scan_kernel<<<1u << dbits, 256, 0, s>>>(w.counts, w.num_tiles, w.bin_total);
-        radix_scatter_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, sizeof(ScatterSmem), s>>>(
+        radix_hist_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, 0, ks>>>(w.keys[cur], a.nnz, shift,
+                                                                                      dbits, w.counts, w.num_tiles);
+        radix_scan_kernel<<<1u << dbits, 256, 0, ks>>>(w.counts, w.num_tiles, w.bin_total);
+        radix_scatter_kernel<<<static_cast<unsigned>(w.num_tiles), kSortThreads, sizeof(ScatterSmem), ks>>>(
             w.keys[cur], w.vals[cur], w.keys[cur ^ 1], w.vals[cur ^ 1], a.nnz, shift, dbits, w.counts, w.num_tiles,
             w.bin_total);
         cur ^= 1;
     }
+    *sorted = cur;
+    return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
+}
+
+template <int D, typename TI>
+dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
+{
+    std::lock_guard<std::mutex> lock(g_side_mutex);
+    SideStream* side = a.nnz > 0 ? side_stream() : nullptr;
+    if (side && (cudaEventRecord(side->fork, s) != cudaSuccess ||
+                 cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess))
+        return DLRM_ERR_CUDA;
+    const cudaStream_t ks = side ? side->stream : s;
+
+    int cur = 0;
+    dlrm_status st = a.nnz > 0 ? sort_keys<TI>(a, w, ks, &cur) : DLRM_OK;
+    // interaction backward (warps per sample: one per 8-row block of dV up to 4 (N <= 32), else 8; a
+    // sample's V is staged once)
+    if (st == DLRM_OK) {
+        const int nblk = round_up(a.T + 1, 8) / 8;
+        st = nblk > 4   ? launch_interact_bwd<D, 8, TI>(a, w.dP, s)
+             : nblk > 2 ? launch_interact_bwd<D, 4, TI>(a, w.dP, s)
+                        : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
+    }
+    // the side stream's work joins the caller's stream whatever happened above
+    if (side && (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+                 cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess))
+        return DLRM_ERR_CUDA;
+    if (st != DLRM_OK || a.nnz == 0) return st;
+
     const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + kSegThreads / kWarp - 1) / (kSegThreads / kWarp));
     segment_chunk_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], w.dP, w.partial,
                                                                w.num_chunks);
