@@ -160,7 +160,13 @@ dlrm_status dlrm_sparse_bwd_workspace_size(const dlrm_tables *tables,
  * has V_t fp32 entries, updated in place.  dense, pooled_saved (device,
  * B x T x D from dlrm_sparse_fwd), grad_out (device, B x (D+N(N-1)/2)),
  * grad_dense (device, B x D, written).  workspace: device, at least
- * dlrm_sparse_bwd_workspace_size() bytes, 16-byte aligned, contents ignored. */
+ * dlrm_sparse_bwd_workspace_size() bytes, 16-byte aligned, contents ignored.
+ * Ordering: the step is one operation on `stream`, after the work queued on
+ * it before the call and before the work queued after.  Inside, the sort of
+ * step 2 runs beside step 1 on a stream the library owns, one per device,
+ * forked from `stream` and joined back to it with events.  The first call on
+ * a device creates that stream; make it before any stream capture.  Host
+ * threads calling at the same time are serialised while they queue work. */
 dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables *tables, const dlrm_bags *bags,
                                     dlrm_pool_mode mode, const float *dense,
                                     const float *pooled_saved,
