@@ -126,16 +126,21 @@ __device__ void pool_bag_warp(const TE* __restrict__ table, int64_t V_t, const v
                 if (!ok[u]) continue;
 #pragma unroll
                 for (int k = 0; k < CPL; ++k) {
+                    // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
+                    float f[EPC];
                     if constexpr (sizeof(TE) == 4) {
-                        acc[k][0] += __uint_as_float(raw[u][k].x);
-                        acc[k][1] += __uint_as_float(raw[u][k].y);
-                        acc[k][2] += __uint_as_float(raw[u][k].z);
-                        acc[k][3] += __uint_as_float(raw[u][k].w);
+                        f[0] = __uint_as_float(raw[u][k].x);
+                        f[1] = __uint_as_float(raw[u][k].y);
+                        f[2] = __uint_as_float(raw[u][k].z);
+                        f[3] = __uint_as_float(raw[u][k].w);
                     } else {
-                        float f[8];
                         bf16x8_to_f32(raw[u][k], f);
+                    }
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[k][e] += f[e];
+                    for (int e = 0; e < EPC; e += 2) {
+                        const float2 s2 = __fadd2_rn(make_float2(acc[k][e], acc[k][e + 1]), make_float2(f[e], f[e + 1]));
+                        acc[k][e] = s2.x;
+                        acc[k][e + 1] = s2.y;
                     }
                 }
             }

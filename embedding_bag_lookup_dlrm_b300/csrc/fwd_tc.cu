@@ -473,11 +473,10 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
                         if ((vmask >> (h + u)) & 1u) {
                             float f[4];
                             widen<4, TE>(raw[u], f);
-                            if ((started >> cur) & 1u) {
-                                acc.x += f[0];
-                                acc.y += f[1];
-                                acc.z += f[2];
-                                acc.w += f[3];
+                            if ((started >> cur) & 1u) {  // packed adds: each lane an fp32 add, rounded once
+                                const float2 a01 = __fadd2_rn(make_float2(acc.x, acc.y), make_float2(f[0], f[1]));
+                                const float2 a23 = __fadd2_rn(make_float2(acc.z, acc.w), make_float2(f[2], f[3]));
+                                acc = make_float4(a01.x, a01.y, a23.x, a23.y);
                             } else {  // a sum starts from its first term
                                 acc = make_float4(f[0], f[1], f[2], f[3]);
                                 started |= 1u << cur;
