@@ -553,6 +553,23 @@ struct Lanes {
     static constexpr int kActive = D >= 128 ? kWarp : D / 4;
 };
 
+// w - step * g, each element one fused multiply-add (as fmaf), two at a time (fma.rn.f32x2).
+__device__ __forceinline__ float4 step_row(float4 w, float4 g, float step)
+{
+    const float2 ns = make_float2(-step, -step);
+    const float2 a = __ffma2_rn(ns, make_float2(g.x, g.y), make_float2(w.x, w.y));
+    const float2 b = __ffma2_rn(ns, make_float2(g.z, g.w), make_float2(w.z, w.w));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// g += v, elementwise, two at a time (add.f32x2: each an fp32 add rounded once).
+__device__ __forceinline__ void add4(float4& g, float4 v)
+{
+    const float2 a = __fadd2_rn(make_float2(g.x, g.y), make_float2(v.x, v.y));
+    const float2 b = __fadd2_rn(make_float2(g.z, g.w), make_float2(v.z, v.w));
+    g = make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <int D>
 __device__ __forceinline__ void adagrad_row(const BwdArgs& a, uint32_t key, int t, const float4 (&g)[Lanes<D>::kChunks],
                                             int lane)
@@ -576,10 +593,7 @@ __device__ __forceinline__ void adagrad_row(const BwdArgs& a, uint32_t key, int 
         for (int k = 0; k < C; ++k) {
             const int col = (lane + k * kWarp) * 4;
             float4 v = *reinterpret_cast<float4*>(w + col);
-            v.x = fmaf(-step, g[k].x, v.x);
-            v.y = fmaf(-step, g[k].y, v.y);
-            v.z = fmaf(-step, g[k].z, v.z);
-            v.w = fmaf(-step, g[k].w, v.w);
+            v = step_row(v, g[k], step);
             *reinterpret_cast<float4*>(w + col) = v;
         }
     }
@@ -618,11 +632,7 @@ __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, in
         float* wr = a.tables[t] + r * D;
 #pragma unroll
         for (int k = 0; k < C; ++k) {
-            float4 v = w[k];
-            v.x = fmaf(-step, g[k].x, v.x);
-            v.y = fmaf(-step, g[k].y, v.y);
-            v.z = fmaf(-step, g[k].z, v.z);
-            v.w = fmaf(-step, g[k].w, v.w);
+            const float4 v = step_row(w[k], g[k], step);
             *reinterpret_cast<float4*>(wr + (lane + k * kWarp) * 4) = v;
         }
     }
@@ -730,12 +740,7 @@ __global__ void __launch_bounds__(kSegThreads, D >= 256 ? 4 : 8) segment_chunk_k
                 }
                 if (active) {
 #pragma unroll
-                    for (int k = 0; k < C; ++k) {
-                        g[k].x += row[u][k].x;
-                        g[k].y += row[u][k].y;
-                        g[k].z += row[u][k].z;
-                        g[k].w += row[u][k].w;
-                    }
+                    for (int k = 0; k < C; ++k) add4(g[k], row[u][k]);
                 }
             }
         }
@@ -783,12 +788,7 @@ __global__ void __launch_bounds__(kSegThreads) segment_span_kernel(const __grid_
     for (int k = 0; k < C; ++k) g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     auto add = [&](const float4 (&v)[C]) {
 #pragma unroll
-        for (int k = 0; k < C; ++k) {
-            g[k].x += v[k].x;
-            g[k].y += v[k].y;
-            g[k].z += v[k].z;
-            g[k].w += v[k].w;
-        }
+        for (int k = 0; k < C; ++k) add4(g[k], v[k]);
     };
     auto load = [&](int64_t slot, float4 (&v)[C]) {
         const float* src = partial + slot * D;
