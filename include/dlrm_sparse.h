@@ -66,14 +66,14 @@ enum {
     DLRM_ERR_BAD_OFFSETS = 4,  /* device: malformed CSR offsets */
     DLRM_ERR_TIMEOUT = 8,      /* device: a bounded wait gave up (work of that sample skipped) */
     DLRM_ERR_CUDA = 16,        /* a CUDA launch or copy returned an error */
-    DLRM_ERR_UNSUPPORTED = 32  /* valid request this build does not implement */
+    DLRM_ERR_UNSUPPORTED = 32  /* valid request the library does not implement */
 };
 
 typedef enum { DLRM_POOL_SUM = 0, DLRM_POOL_MEAN = 1 } dlrm_pool_mode;
 typedef enum { DLRM_F32 = 0, DLRM_BF16 = 1 } dlrm_dtype;
 typedef enum { DLRM_I32 = 0, DLRM_I64 = 1 } dlrm_index_type;
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define DLRM_MAX_TABLES 128
 
 /* The embedding tables.  num_tables = T in [1, DLRM_MAX_TABLES]; dim = D in

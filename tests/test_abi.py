@@ -66,7 +66,7 @@ def test_host_argument_checks(lib):
     assert lib.dlrm_sparse_fwd(ctypes.byref(bad_T), ctypes.byref(bags), 0, 0x4000, 0x5000, None, None, None) == 1
     bad_D, _a, _b = _tables(D=130)
     assert lib.dlrm_embbag_fwd(ctypes.byref(bad_D), ctypes.byref(bags), 0, 0x4000, None, None) == 1
-    odd_D, _a, _b = _tables(D=48)   # a multiple of 4 this build has no kernel for
+    odd_D, _a, _b = _tables(D=48)   # a multiple of 4 the library has no kernel for
     assert lib.dlrm_embbag_fwd(ctypes.byref(odd_D), ctypes.byref(bags), 0, 0x4000, None, None) == \
         dl.DLRM_ERR_UNSUPPORTED
     misaligned, _a, _b = _tables(ptr=0x1004)
