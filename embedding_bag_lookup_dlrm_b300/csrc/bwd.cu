@@ -651,7 +651,8 @@ __global__ void __launch_bounds__(kSegThreads, D >= 256 ? 4 : 8) segment_chunk_k
                                                                        float* __restrict__ partial, int64_t num_chunks)
 {
     constexpr int C = Lanes<D>::kChunks;
-    constexpr int U = 2;  // lookups per group
+    constexpr int U = 2;  // lookups per group: small, since more warps per SM (8 CTAs) hide this kernel's
+                          // chains of dependent instructions better than deeper loads do
     const int lane = threadIdx.x & 31;
     const int64_t chunk = blockIdx.x * int64_t{blockDim.x / kWarp} + (threadIdx.x >> 5);
     if (chunk >= num_chunks) return;

@@ -14,8 +14,11 @@
 //     mbarrier), so a warp has every row of its sample in flight at once;
 //   * multi-hot or bf16 bags are pooled in registers: each lane owns one or
 //     more 16-byte chunks of a row, several rows per load instruction when a
-//     row is narrower than a warp, 8-16 rows in flight per warp, fp32
-//     accumulation in lookup order;
+//     row is narrower than a warp, up to 16 load instructions in flight per
+//     warp (16 fp32 or 32 bf16 rows at D = 128), fp32 accumulation in lookup
+//     order (packed fp32 adds, each rounded as a scalar add); when bags
+//     average 8 or more lookups, two warps share a sample and take its bags
+//     alternately;
 //   * the strict upper triangle of V V^T is computed by register-blocked FFMA:
 //     the rows are split into 4-row blocks with stride NB (block k = rows
 //     k, k+NB, k+2NB, k+3NB) so that the lanes of a warp, each owning one

@@ -14,14 +14,18 @@
 // a tile holds S = 128 / NP samples.  Warp w gathers tile rows 32w..32w+31
 // and later reads the same rows of the Gram back from its quarter of TMEM.
 //
-// Gather.  A warp flattens the lookups of its 32 rows into one list and
-// loads them 16 at a time (each lane one 4- to 16-byte slice of a row, the
-// warp one whole row per load instruction), so a one-hot tile and a tile of
-// long bags keep the same number of rows in flight.  Each lookup is added
-// into its row in lookup order in fp32; a finished row (the pooled vector)
-// is written once, as a pair of bf16 (hi = bf16(v), lo = bf16(v - hi)) into
-// two K-major, 128-byte-swizzled operand buffers in shared memory, and to
-// pooled_save when asked.  x is also staged exactly for the output row.
+// Gather.  Rows with a single source (x, bags of one lookup, the pooled
+// inputs of the interaction-only call) are copied by 16-byte cp.async
+// straight into the operand lines, every such row of the warp in flight at
+// once.  In the multi-lookup variant (bags of more than 1.25 lookups on
+// average) a warp flattens the lookups of its other rows into one list and
+// loads them 16 at a time (each lane a 16-byte slice of a row, the warp one
+// whole row per load instruction), each added into its row in lookup order in
+// fp32 (packed adds, each rounded as a scalar add).  A finished row (the
+// pooled vector) is written once, as a pair of bf16 (hi = bf16(v),
+// lo = bf16(v - hi)) into two K-major, 128-byte-swizzled operand buffers in
+// shared memory, and to pooled_save when asked.  x is also staged exactly for
+// the output row.
 //
 // Gram.  One thread issues, for the tile, hi*hi^T + hi*lo^T + lo*hi^T as
 // 3 x D/16 MMAs of 128 x 128 x 16 into one 128 x 128 fp32 accumulator in
