@@ -88,21 +88,20 @@ __device__ __forceinline__ int64_t ld_index(const void* p, int64_t i)
 // ---------------------------------------------------------------------------
 // 1. Interaction backward.  One group of G warps per sample.  V (x, then the
 // pooled rows) arrives by two bulk copies; the symmetric upstream matrix g
-// (zero diagonal) is built in shared memory from the triangle, each entry
-// stored twice as a float2 so that one broadcast 16-byte load feeds two packed
-// fp32 FMAs (fma.rn.f32x2: two independent fused multiply-adds, each rounded
-// once, as fmaf); where that copy of g does not fit in shared memory, g is
-// stored once and the FMAs are scalar.  Each lane owns 16-byte column chunks
-// of V and accumulates an 8-row block of dV = g V, summing over j in
-// increasing order.
+// (zero diagonal) is built in shared memory from the triangle.  Each lane owns
+// 16-byte column chunks of V and accumulates an 8-row block of dV = g V,
+// summing over j in increasing order, with packed fp32 FMAs (fma.rn.f32x2:
+// two independent fused multiply-adds, each rounded once, as fmaf) on pairs of
+// rows: one broadcast 16-byte load of g gives the factors of four rows, and
+// each V value is paired with itself in registers.  Shared-memory bandwidth
+// bounds this kernel, so g is kept once and the pairing is done in registers.
 // ---------------------------------------------------------------------------
 struct BwdLayout {
     int N, NP, K, W;  // NP = N rounded up to 8 (rows of g); W = D + K (upstream row)
     int off_V, off_g, off_go, bytes;
 };
 
-// pair: g stored as float2 (g, g) per entry for the packed FMAs, else as float
-__host__ __device__ inline BwdLayout make_bwd_layout(int T, int D, bool pair)
+__host__ __device__ inline BwdLayout make_bwd_layout(int T, int D)
 {
     BwdLayout l;
     l.N = T + 1;
@@ -113,7 +112,7 @@ __host__ __device__ inline BwdLayout make_bwd_layout(int T, int D, bool pair)
     l.off_V = o;
     o += 4 * l.N * D;
     l.off_g = o;
-    o += (pair ? 8 : 4) * l.NP * l.NP;
+    o += 4 * l.NP * l.NP;
     l.off_go = o;
     o += 4 * l.W;
     l.bytes = round_up(o, 128);
@@ -122,7 +121,7 @@ __host__ __device__ inline BwdLayout make_bwd_layout(int T, int D, bool pair)
 
 // In mean mode dP[b][t] is stored already divided by the bag length L (the
 // scale every lookup of the bag applies), so the per-row sums are plain sums.
-template <int D, int G, typename TI, bool PAIR>
+template <int D, int G, typename TI>
 __global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) interact_bwd_kernel(const __grid_constant__ BwdArgs a, float* __restrict__ dP,
                                                            int groups_per_cta)
 {
@@ -132,7 +131,7 @@ __global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) inte
     constexpr int LPR = CPR < kWarp ? CPR : kWarp;   // lanes per row
     constexpr int CPL = CPR / LPR;                   // chunks per lane
     constexpr int RPI = kWarp / LPR;                 // row blocks worked on side by side
-    const BwdLayout l = make_bwd_layout(a.T, D, PAIR);
+    const BwdLayout l = make_bwd_layout(a.T, D);
     const int group = threadIdx.x / GT;
     const int gl = threadIdx.x % GT;
     const int lane = gl % kWarp;
@@ -169,10 +168,7 @@ __global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) inte
         for (int e = gl; e < NP * NP; e += GT) {
             float v = 0.0f;
             if (i < N && j < N && i != j) v = tri[i < j ? tri_index(i, j, N) : tri_index(j, i, N)];
-            if constexpr (PAIR)
-                reinterpret_cast<float2*>(gm)[e] = make_float2(v, v);
-            else
-                gm[e] = v;
+            gm[e] = v;
             i += di;
             j += dj;
             if (j >= NP) {
@@ -200,43 +196,29 @@ __global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) inte
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
             const int col = (c0 + c * LPR) * 4;
+            float2 p[4][4];  // p[q][c]: rows i0 + 2q, i0 + 2q + 1 at column col + c
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) p[q][c4] = make_float2(0.f, 0.f);
+            for (int j = 0; j < N; ++j) {
+                const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
+                const float4 g0 = *reinterpret_cast<const float4*>(gm + j * NP + i0);
+                const float4 g1 = *reinterpret_cast<const float4*>(gm + j * NP + i0 + 4);
+                const float2 gq[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w), make_float2(g1.x, g1.y),
+                                      make_float2(g1.z, g1.w)};
+                const float2 vv[4] = {make_float2(v.x, v.x), make_float2(v.y, v.y), make_float2(v.z, v.z),
+                                      make_float2(v.w, v.w)};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) p[q][c4] = __ffma2_rn(gq[q], vv[c4], p[q][c4]);
+            }
             float4 acc[8];
-            if constexpr (PAIR) {
-                float2 lo[8], hi[8];  // row i0 + r: columns col, col+1 and col+2, col+3
 #pragma unroll
-                for (int r = 0; r < 8; ++r) lo[r] = hi[r] = make_float2(0.f, 0.f);
-                for (int j = 0; j < N; ++j) {
-                    const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
-                    const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
-                    const float4* gj = reinterpret_cast<const float4*>(gm + 2 * (j * NP + i0));
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 g2 = gj[q];  // (g, g) of rows i0 + 2q and i0 + 2q + 1
-                        const float2 ga = make_float2(g2.x, g2.y), gb = make_float2(g2.z, g2.w);
-                        lo[2 * q] = __ffma2_rn(ga, v01, lo[2 * q]);
-                        hi[2 * q] = __ffma2_rn(ga, v23, hi[2 * q]);
-                        lo[2 * q + 1] = __ffma2_rn(gb, v01, lo[2 * q + 1]);
-                        hi[2 * q + 1] = __ffma2_rn(gb, v23, hi[2 * q + 1]);
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < 8; ++r) acc[r] = make_float4(lo[r].x, lo[r].y, hi[r].x, hi[r].y);
-            } else {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int j = 0; j < N; ++j) {
-                    const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
-                    const float4 g0 = *reinterpret_cast<const float4*>(gm + j * NP + i0);
-                    const float4 g1 = *reinterpret_cast<const float4*>(gm + j * NP + i0 + 4);
-                    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        acc[r].x = fmaf(gg[r], v.x, acc[r].x);
-                        acc[r].y = fmaf(gg[r], v.y, acc[r].y);
-                        acc[r].z = fmaf(gg[r], v.z, acc[r].z);
-                        acc[r].w = fmaf(gg[r], v.w, acc[r].w);
-                    }
-                }
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] = make_float4(p[q][0].x, p[q][1].x, p[q][2].x, p[q][3].x);
+                acc[2 * q + 1] = make_float4(p[q][0].y, p[q][1].y, p[q][2].y, p[q][3].y);
             }
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -818,10 +800,10 @@ __global__ void __launch_bounds__(kSegThreads) segment_span_kernel(const __grid_
 // ---------------------------------------------------------------------------
 constexpr int kMaxSmem = 227 * 1024;
 
-template <int D, int G, typename TI, bool PAIR>
-dlrm_status launch_interact_bwd_as(const BwdArgs& a, float* dP, cudaStream_t s)
+template <int D, int G, typename TI>
+dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
 {
-    const BwdLayout l = make_bwd_layout(a.T, D, PAIR);
+    const BwdLayout l = make_bwd_layout(a.T, D);
     int groups = 1;
     if (G == 1) {
         groups = kMaxSmem / l.bytes;
@@ -831,20 +813,12 @@ dlrm_status launch_interact_bwd_as(const BwdArgs& a, float* dP, cudaStream_t s)
         return DLRM_ERR_UNSUPPORTED;
     }
     const size_t smem = static_cast<size_t>(groups) * l.bytes;
-    auto kern = interact_bwd_kernel<D, G, TI, PAIR>;
+    auto kern = interact_bwd_kernel<D, G, TI>;
     if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
         return DLRM_ERR_CUDA;
     const int64_t blocks = (a.B + groups - 1) / groups;
     kern<<<static_cast<unsigned>(blocks), groups * G * kWarp, smem, s>>>(a, dP, groups);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
-}
-
-// g as float2 pairs for the packed FMAs when that layout fits in shared memory, else as floats
-template <int D, int G, typename TI>
-dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
-{
-    return make_bwd_layout(a.T, D, true).bytes <= kMaxSmem ? launch_interact_bwd_as<D, G, TI, true>(a, dP, s)
-                                                           : launch_interact_bwd_as<D, G, TI, false>(a, dP, s);
 }
 
 // The lookup keys are built and sorted on a second stream of the device while

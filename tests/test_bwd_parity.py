@@ -81,7 +81,7 @@ CASES = [
     (16, 3, "mean", "i32", 1, 3, 1000, 7),
     (256, 2, "sum", "i64", 1, 1, 33, 1000),
     (32, 100, "sum", "i32", 1, 2, 21, 100),
-    # N = 113 at D = 256: g stored once (the paired copy would not fit), scalar FMAs
+    # N = 113 at D = 256: eight warps per sample, close to the largest shared-memory layout
     (256, 112, "mean", "i32", 0, 2, 9, 50),
 ]
 
