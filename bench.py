@@ -516,7 +516,7 @@ def forward_kernel_name(w):
     mean_len = (w.bag_max + w.bag_min) / 2
     tc = w.D in (64, 128) and w.T + 1 <= 128 and mean_len <= 16
     if not tc:
-        return "forward_kernel (fused sparse forward, FFMA Gram)"
+        return "forward_kernel (fused sparse forward, FFMA Gram" + (", two warps per sample)" if mean_len >= 8 else ")")
     return ("forward_tc_kernel (fused sparse forward, tcgen05 Gram"
             + (", multi-lookup bags)" if mean_len > 1.25 else ")"))
 
