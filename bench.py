@@ -418,9 +418,12 @@ def run_ours(args, w):
         if mid is not None:
             mid.record(s)
         dl.dlrm_sparse_bwd_adagrad(tables, accum, idx, off, x, pooled, grads[i % N_ROTATE], w.lr, w.eps, w.mode,
-                                   grad_dense=grad_dense, workspace=workspace, stream=s)
+                                   grad_dense=grad_dense, workspace=workspace, stream=s, side_stream=side)
 
     s = torch.cuda.Stream(device=dev)
+    # the training step's key build and sort run beside its interaction backward, on a stream of the
+    # highest priority so that the short dependent sort kernels get SMs as soon as any free up
+    side = torch.cuda.Stream(device=dev, priority=-100)
     with torch.cuda.stream(s):
         for i in range(args.warmup):
             flush_l2()
@@ -529,6 +532,7 @@ def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):
             for b in batches]
     max_nnz = max(b.nnz for b in batches)
     comp, copy = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    side = torch.cuda.Stream(device=dev, priority=-100)
     stages = []
     for _ in range(2):
         stages.append((torch.empty(max_nnz, dtype=torch.int32, device=dev),
@@ -568,7 +572,7 @@ def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):
         comp.wait_event(copied[k])
         dl.dlrm_sparse_fwd(tables, di[:hi.numel()], do, dx, w.mode, out=out, pooled_save=pooled, stream=comp)
         dl.dlrm_sparse_bwd_adagrad(tables, accum, di[:hi.numel()], do, dx, pooled, dg, w.lr, w.eps, w.mode,
-                                   grad_dense=gd, workspace=ws, stream=comp)
+                                   grad_dense=gd, workspace=ws, stream=comp, side_stream=side)
         with torch.cuda.stream(comp):
             gd_host[k].copy_(gd, non_blocking=True)
         ev = torch.cuda.Event()

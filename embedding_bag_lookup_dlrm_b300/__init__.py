@@ -74,7 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dlrm_sparse_fwd_host": ([T, B, i32, P, P, P, P, P, P, P, P], i32),
         "dlrm_sparse_bwd_workspace_size": ([T, B, ctypes.POINTER(ctypes.c_size_t)], i32),
         "dlrm_sparse_bwd_adagrad": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p), ctypes.c_float,
-                                     ctypes.c_float, P, ctypes.c_size_t, P, P], i32),
+                                     ctypes.c_float, P, ctypes.c_size_t, P, P, P], i32),
         "dlrm_sparse_bwd_adagrad_static": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p),
                                             ctypes.c_float, ctypes.c_float, P, P], i32),
         "dlrm_status_string": ([i32], ctypes.c_char_p),
@@ -98,9 +98,19 @@ def status_string(status: int) -> str:
 # ---------------------------------------------------------------------------
 # marshalling helpers
 # ---------------------------------------------------------------------------
-def _stream_ptr(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _stream_ptr(stream, device) -> int:
+    """The stream to queue on: the given one, else the current stream of `device`."""
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return s.cuda_stream
+
+
+def _device(*tensors) -> torch.device:
+    """The one CUDA device all given tensors live on (the C library runs on the current device, so every
+    call is made with this device current)."""
+    devs = {t.device for t in tensors if isinstance(t, torch.Tensor) and t.is_cuda}
+    if len(devs) != 1:
+        raise ValueError(f"tensors must live on one CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
 
 
 def _check_cuda(t: torch.Tensor, name: str, dtype=None):
@@ -171,8 +181,10 @@ def dlrm_embbag_fwd(tables, indices, offsets, mode="sum", pooled=None, status=No
         pooled = torch.empty((B, tb.T, tb.D), dtype=torch.float32, device=indices.device)
     _check_cuda(pooled, "pooled", torch.float32)
     bags = _bags(indices, offsets, B)
-    st = lib.dlrm_embbag_fwd(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], pooled.data_ptr(),
-                             status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    dev = _device(*tb.tensors, indices, offsets, pooled, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_embbag_fwd(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], pooled.data_ptr(),
+                                 status.data_ptr() if status is not None else None, _stream_ptr(stream, dev))
     _raise(st, "dlrm_embbag_fwd")
     return pooled
 
@@ -187,7 +199,10 @@ def dlrm_interact_fwd(dense, pooled, out=None, stream=None):
     if out is None:
         out = torch.empty((B, D + N * (N - 1) // 2), dtype=torch.float32, device=dense.device)
     _check_cuda(out, "out", torch.float32)
-    st = lib.dlrm_interact_fwd(dense.data_ptr(), pooled.data_ptr(), B, T, D, out.data_ptr(), _stream_ptr(stream))
+    dev = _device(dense, pooled, out)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_interact_fwd(dense.data_ptr(), pooled.data_ptr(), B, T, D, out.data_ptr(),
+                                   _stream_ptr(stream, dev))
     _raise(st, "dlrm_interact_fwd")
     return out
 
@@ -206,9 +221,11 @@ def dlrm_sparse_fwd(tables, indices, offsets, dense, mode="sum", out=None, poole
     if pooled_save is not None:
         _check_cuda(pooled_save, "pooled_save", torch.float32)
     bags = _bags(indices, offsets, B)
-    st = lib.dlrm_sparse_fwd(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
-                             out.data_ptr(), pooled_save.data_ptr() if pooled_save is not None else None,
-                             status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    dev = _device(*tb.tensors, indices, offsets, dense, out, pooled_save, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_fwd(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
+                                 out.data_ptr(), pooled_save.data_ptr() if pooled_save is not None else None,
+                                 status.data_ptr() if status is not None else None, _stream_ptr(stream, dev))
     _raise(st, "dlrm_sparse_fwd")
     return out
 
@@ -238,10 +255,12 @@ def dlrm_sparse_fwd_host(tables, indices_host, offsets_host, dense_host, out_hos
     if staging.indices.numel() < indices_host.numel() or staging.offsets.numel() < offsets_host.numel():
         raise ValueError("staging buffers too small")
     bags = _bags(indices_host, offsets_host, B, device=False)
-    st = lib.dlrm_sparse_fwd_host(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense_host.data_ptr(),
-                                  out_host.data_ptr(), staging.indices.data_ptr(), staging.offsets.data_ptr(),
-                                  staging.dense.data_ptr(), staging.out.data_ptr(),
-                                  status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    dev = _device(*tb.tensors, staging.indices, staging.offsets, staging.dense, staging.out, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_fwd_host(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense_host.data_ptr(),
+                                      out_host.data_ptr(), staging.indices.data_ptr(), staging.offsets.data_ptr(),
+                                      staging.dense.data_ptr(), staging.out.data_ptr(),
+                                      status.data_ptr() if status is not None else None, _stream_ptr(stream, dev))
     _raise(st, "dlrm_sparse_fwd_host")
     return out_host
 
@@ -258,9 +277,10 @@ def dlrm_sparse_bwd_workspace_size(tables, indices, offsets) -> int:
 
 
 def dlrm_sparse_bwd_adagrad(tables, accum, indices, offsets, dense, pooled_saved, grad_out, lr, eps, mode="sum",
-                            grad_dense=None, workspace=None, status=None, stream=None):
+                            grad_dense=None, workspace=None, status=None, stream=None, side_stream=None):
     """One training step of the sparse path; tables and accum are updated in place.
-    Returns grad_dense [B, D]."""
+    side_stream (optional, same device): runs the lookup-key build and sort beside the
+    interaction backward.  Returns grad_dense [B, D]."""
     lib = load_library()
     tb = _tables(tables)
     B = _batch(offsets, tb.T)
@@ -281,10 +301,15 @@ def dlrm_sparse_bwd_adagrad(tables, accum, indices, offsets, dense, pooled_saved
     _check_cuda(workspace, "workspace")
     acc_ptrs = (ctypes.c_void_p * tb.T)(*[a.data_ptr() for a in accum])
     bags = _bags(indices, offsets, B)
-    st = lib.dlrm_sparse_bwd_adagrad(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
-                                     pooled_saved.data_ptr(), grad_out.data_ptr(), grad_dense.data_ptr(), acc_ptrs,
-                                     float(lr), float(eps), workspace.data_ptr(), workspace.numel(),
-                                     status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    dev = _device(*tb.tensors, *accum, indices, offsets, dense, pooled_saved, grad_out, grad_dense, workspace,
+                  status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_bwd_adagrad(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
+                                         pooled_saved.data_ptr(), grad_out.data_ptr(), grad_dense.data_ptr(),
+                                         acc_ptrs, float(lr), float(eps), workspace.data_ptr(), workspace.numel(),
+                                         status.data_ptr() if status is not None else None,
+                                         _stream_ptr(stream, dev),
+                                         side_stream.cuda_stream if side_stream is not None else None)
     _raise(st, "dlrm_sparse_bwd_adagrad")
     return grad_dense
 
@@ -316,10 +341,12 @@ def dlrm_sparse_bwd_adagrad_static(tables, accum, indices, offsets, dense, poole
     _check_cuda(grad_dense, "grad_dense", torch.float32)
     acc_ptrs = (ctypes.c_void_p * tb.T)(*[a.data_ptr() for a in accum])
     bags = _bags(indices, offsets, B)
-    st = lib.dlrm_sparse_bwd_adagrad_static(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode],
-                                            dense.data_ptr(), pooled_saved.data_ptr(), grad_out.data_ptr(),
-                                            grad_dense.data_ptr(), acc_ptrs, float(lr), float(eps),
-                                            status.data_ptr() if status is not None else None,
-                                            _stream_ptr(stream))
+    dev = _device(*tb.tensors, *accum, indices, offsets, dense, pooled_saved, grad_out, grad_dense, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_bwd_adagrad_static(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode],
+                                                dense.data_ptr(), pooled_saved.data_ptr(), grad_out.data_ptr(),
+                                                grad_dense.data_ptr(), acc_ptrs, float(lr), float(eps),
+                                                status.data_ptr() if status is not None else None,
+                                                _stream_ptr(stream, dev))
     _raise(st, "dlrm_sparse_bwd_adagrad_static")
     return grad_dense

@@ -64,7 +64,7 @@ int64_t out_width(int32_t T, int32_t D) { return D + int64_t{T + 1} * T / 2; }
 
 extern "C" {
 
-int32_t dlrm_abi_version(void) { return 1; }
+int32_t dlrm_abi_version(void) { return 2; }
 
 const char* dlrm_status_string(dlrm_status s)
 {
@@ -172,7 +172,8 @@ dlrm_status dlrm_sparse_bwd_workspace_size(const dlrm_tables* tables, const dlrm
 dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
                                     const float* dense, const float* pooled_saved, const float* grad_out,
                                     float* grad_dense, float* const* accum, float lr, float eps, void* workspace,
-                                    size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream)
+                                    size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
+                                    cudaStream_t side_stream)
 {
     dlrm_status st = check_tables(tables);
     if (st != DLRM_OK) return st;
@@ -189,7 +190,11 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* 
         for (int i = 0; i < tables->num_tables; ++i) s += tables->num_rows[i];
         return s;
     }();
-    if (total_rows >= (int64_t{1} << 32) - 1) return DLRM_ERR_UNSUPPORTED;  // sort keys are 32-bit
+    // 32-bit sort keys (global row ids, the sentinel 2^32 - 1 above them), 32-bit sort values (dP row
+    // b*T + t) and 32-bit positions in the sorted lookups
+    if (total_rows >= (int64_t{1} << 32) - 1) return DLRM_ERR_UNSUPPORTED;
+    if (int64_t{tables->num_tables} * bags->batch >= (int64_t{1} << 32)) return DLRM_ERR_UNSUPPORTED;
+    if (bags->nnz >= (int64_t{1} << 32)) return DLRM_ERR_UNSUPPORTED;
     if (workspace_bytes < dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz))
         return DLRM_ERR_INVALID_ARG;
     BwdArgs a;
@@ -218,7 +223,8 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* 
     a.lr = lr;
     a.eps = eps;
     a.t_magic = a.T >= 2 ? ~uint64_t{0} / static_cast<uint64_t>(a.T) + 1 : 0;
-    return dlrm::launch_backward(a, tables->dim, bags->index_type, workspace, workspace_bytes, stream);
+    return dlrm::launch_backward(a, tables->dim, bags->index_type, workspace, workspace_bytes, stream,
+                                 side_stream);
 }
 
 }  // extern "C"

@@ -13,8 +13,6 @@
 // added in chunk order), so two calls on the same inputs give the same bits.
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -821,45 +819,6 @@ dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
-// The lookup keys are built and sorted on a second stream of the device while
-// the interaction backward runs on the caller's stream: the two read the same
-// inputs and write disjoint parts of the workspace, and only the per-row sums
-// need both.  Fork and join are events, so the pattern also holds while the
-// caller's stream is being captured into a CUDA graph.  The side stream runs
-// at the device's highest priority so that the short, dependent sort kernels
-// get SMs as soon as the interaction backward frees them.
-struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-    bool tried = false;
-};
-std::mutex g_side_mutex;  // held while a call enqueues its fork and join (the events are per device)
-SideStream g_side[64];
-
-// The device's side stream, created on first use; nullptr if it cannot be made (the sort then runs on the
-// caller's stream).  Called with g_side_mutex held.
-SideStream* side_stream()
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    SideStream& sd = g_side[dev];
-    if (!sd.tried) {
-        sd.tried = true;
-        int least = 0, greatest = 0;
-        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&sd.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
-            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
-            if (sd.join) cudaEventDestroy(sd.join);
-            if (sd.fork) cudaEventDestroy(sd.fork);
-            if (sd.stream) cudaStreamDestroy(sd.stream);
-            sd = SideStream{nullptr, nullptr, nullptr, true};
-            cudaGetLastError();  // clear the failure: the call goes on on one stream
-        }
-    }
-    return sd.stream ? &sd : nullptr;
-}
-
 // Keys, then the stable radix sort, on stream ks; returns the ping-pong buffer holding the sorted pairs.
 template <typename TI>
 dlrm_status sort_keys(const BwdArgs& a, const Workspace& w, cudaStream_t ks, int* sorted)
@@ -876,13 +835,10 @@ dlrm_status sort_keys(const BwdArgs& a, const Workspace& w, cudaStream_t ks, int
     while ((int64_t{1} << bits) <= a.row_base[a.T]) ++bits;
     const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
     const int dbits = (bits + passes - 1) / passes;
-    static bool scatter_configured = false;
-    if (!scatter_configured) {
-        if (cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(sizeof(ScatterSmem))) != cudaSuccess)
-            return DLRM_ERR_CUDA;
-        scatter_configured = true;
-    }
+    // set on every call: the attribute belongs to the current device's context
+    if (cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(ScatterSmem))) != cudaSuccess)
+        return DLRM_ERR_CUDA;
     int cur = 0;
     for (int pass = 0; pass < passes; ++pass) {
         const int shift = pass * dbits;
@@ -898,15 +854,33 @@ dlrm_status sort_keys(const BwdArgs& a, const Workspace& w, cudaStream_t ks, int
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
+// The lookup keys can be built and sorted on a second stream while the
+// interaction backward runs on the caller's stream: the two read the same
+// inputs and write disjoint parts of the workspace, and only the per-row sums
+// need both.  The caller supplies that stream (the library owns none); fork
+// and join are two events made for this call and released once queued, so
+// calls on independent streams share nothing, and the pattern also holds
+// while the caller's stream is being captured into a CUDA graph.
+struct Fork {
+    cudaEvent_t fork = nullptr, join = nullptr;
+    ~Fork()
+    {
+        // an event destroyed after being queued is released once the device has passed it
+        if (fork) cudaEventDestroy(fork);
+        if (join) cudaEventDestroy(join);
+    }
+};
+
 template <int D, typename TI>
-dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
+dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s, cudaStream_t side)
 {
-    std::lock_guard<std::mutex> lock(g_side_mutex);
-    SideStream* side = a.nnz > 0 ? side_stream() : nullptr;
-    if (side && (cudaEventRecord(side->fork, s) != cudaSuccess ||
-                 cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess))
+    Fork f;
+    const bool two = side != nullptr && side != s && a.nnz > 0;
+    if (two && (cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventRecord(f.fork, s) != cudaSuccess || cudaStreamWaitEvent(side, f.fork, 0) != cudaSuccess))
         return DLRM_ERR_CUDA;
-    const cudaStream_t ks = side ? side->stream : s;
+    const cudaStream_t ks = two ? side : s;
 
     int cur = 0;
     dlrm_status st = a.nnz > 0 ? sort_keys<TI>(a, w, ks, &cur) : DLRM_OK;
@@ -919,8 +893,7 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
                         : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
     }
     // the side stream's work joins the caller's stream whatever happened above
-    if (side && (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
-                 cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess))
+    if (two && (cudaEventRecord(f.join, side) != cudaSuccess || cudaStreamWaitEvent(s, f.join, 0) != cudaSuccess))
         return DLRM_ERR_CUDA;
     if (st != DLRM_OK || a.nnz == 0) return st;
 
@@ -932,9 +905,9 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s)
 }
 
 template <int D>
-dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, cudaStream_t s)
+dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, cudaStream_t s, cudaStream_t side)
 {
-    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, s) : run_backward<D, int64_t>(a, w, s);
+    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, s, side) : run_backward<D, int64_t>(a, w, s, side);
 }
 
 }  // namespace
@@ -947,17 +920,17 @@ size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz)
 }
 
 dlrm_status launch_backward(const BwdArgs& a, int dim, int index_type, void* workspace, size_t workspace_bytes,
-                            cudaStream_t s)
+                            cudaStream_t s, cudaStream_t side)
 {
     size_t need = 0;
     const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, &need);
     if (workspace_bytes < need) return DLRM_ERR_INVALID_ARG;
     switch (dim) {
-        case 16: return dispatch_bwd<16>(a, index_type, w, s);
-        case 32: return dispatch_bwd<32>(a, index_type, w, s);
-        case 64: return dispatch_bwd<64>(a, index_type, w, s);
-        case 128: return dispatch_bwd<128>(a, index_type, w, s);
-        case 256: return dispatch_bwd<256>(a, index_type, w, s);
+        case 16: return dispatch_bwd<16>(a, index_type, w, s, side);
+        case 32: return dispatch_bwd<32>(a, index_type, w, s, side);
+        case 64: return dispatch_bwd<64>(a, index_type, w, s, side);
+        case 128: return dispatch_bwd<128>(a, index_type, w, s, side);
+        case 256: return dispatch_bwd<256>(a, index_type, w, s, side);
         default: return DLRM_ERR_UNSUPPORTED;
     }
 }

@@ -17,8 +17,6 @@
 // sums), so nothing has to be cleared between calls.  Two calls whose work
 // overlaps on the GPU (different streams, or different host threads without
 // ordering) use the same bytes at once and race; the caller must order them.
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "dlrm_sparse.h"
@@ -26,29 +24,20 @@
 namespace {
 
 constexpr size_t kScratchBytes = DLRM_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // The scratch itself.  In host code `g_scratch` names a host-side stand-in,
 // not device memory: only the address from cudaGetSymbolAddress may be
 // handed to a kernel.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::mutex g_mutex;
-void* g_scratch_dev[kMaxDevices] = {};  // device address of g_scratch, per device ordinal
-
-// Address of g_scratch on the current device, looked up once per device.
+// Address of g_scratch on the current device.  Looked up on every call (a
+// cheap query once the module is loaded), never cached: after a context reset
+// the array lives at a new address.
 dlrm_status scratch_address(void** out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return DLRM_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return DLRM_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_dev[dev] == nullptr) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress((void**)&ptr, g_scratch) != cudaSuccess || ptr == nullptr) return DLRM_ERR_CUDA;
-        g_scratch_dev[dev] = ptr;
-    }
-    *out = g_scratch_dev[dev];
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress((void**)&ptr, g_scratch) != cudaSuccess || ptr == nullptr) return DLRM_ERR_CUDA;
+    *out = ptr;
     return DLRM_OK;
 }
 
@@ -67,5 +56,5 @@ extern "C" dlrm_status dlrm_sparse_bwd_adagrad_static(const dlrm_tables* tables,
     void* scratch = nullptr;
     if ((st = scratch_address(&scratch)) != DLRM_OK) return st;
     return dlrm_sparse_bwd_adagrad(tables, bags, mode, dense, pooled_saved, grad_out, grad_dense, accum, lr, eps,
-                                   scratch, kScratchBytes, status_dev, stream);
+                                   scratch, kScratchBytes, status_dev, stream, nullptr);
 }

@@ -392,12 +392,10 @@ dlrm_status launch_one(const FwdArgs& a, cudaStream_t stream)
     }
     const size_t smem = static_cast<size_t>(groups) * g.bytes;
     auto kern = forward_kernel<D, TE, TI, MODE, G>;
-    static int configured_bytes = 0;  // per instantiation
-    if (smem > 48 * 1024 && static_cast<int>(smem) > configured_bytes) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess)
-            return DLRM_ERR_CUDA;
-        configured_bytes = kMaxSmem;
-    }
+    // set on every launch: the attribute belongs to the current device's context
+    if (smem > 48 * 1024 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+                                cudaSuccess)
+        return DLRM_ERR_CUDA;
     const int64_t blocks = (a.B + groups - 1) / groups;
     if (blocks > 0x7fffffff) return DLRM_ERR_UNSUPPORTED;
     kern<<<static_cast<unsigned>(blocks), groups * G * kWarp, smem, stream>>>(a, groups);

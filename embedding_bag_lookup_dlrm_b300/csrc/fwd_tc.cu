@@ -719,19 +719,6 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kSmemPerSm = 228 * 1024;
 
-int sm_count()
-{
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
-
 template <int D, typename TE, typename TI, int MODE, int NP, bool MULTI>
 dlrm_status launch_tc(const FwdArgs& a, cudaStream_t stream)
 {
@@ -743,19 +730,13 @@ dlrm_status launch_tc(const FwdArgs& a, cudaStream_t stream)
     if (smem < kMinSmemPerCta) smem = kMinSmemPerCta;
     if (smem > kMaxSmem) return DLRM_ERR_UNSUPPORTED;
     auto kern = forward_tc_kernel<D, TE, TI, MODE, NP, MULTI>;
-    static int configured = 0;  // per instantiation
-    if (!configured) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-            return DLRM_ERR_CUDA;
-    }
-    static int regs = 0;  // per instantiation
-    if (!configured) {
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return DLRM_ERR_CUDA;
-        regs = fa.numRegs;
-        configured = 1;
-    }
+    // Function attributes belong to the current device's context: set them on every launch (a cheap host
+    // call), so that every device, and a context made again after a reset, gets them.
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    const int regs = kernel_registers(reinterpret_cast<const void*>(kern));
+    if (regs <= 0) return DLRM_ERR_CUDA;
     // CTAs per SM: shared memory (1 KB of it reserved per CTA), registers, TMEM
     int per_sm = kSmemPerSm / (smem + 1024);
     const int by_regs = 65536 / (round_up(regs, 8) * kThreads);

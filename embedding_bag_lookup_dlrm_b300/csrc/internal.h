@@ -33,6 +33,11 @@ struct FwdArgs {
     int32_t mean;
 };
 
+// Number of SMs of the current device (0 on error).
+int sm_count();
+// Registers per thread of a compiled kernel (0 on error).
+int kernel_registers(const void* kernel);
+
 // Launch one forward pass.  dim in {16,32,64,128,256}; dtype/index_type as in
 // the ABI.  Returns DLRM_OK, DLRM_ERR_UNSUPPORTED or DLRM_ERR_CUDA.
 dlrm_status launch_forward(int mode, const FwdArgs& args, int dim, int dtype, int index_type,
@@ -69,7 +74,8 @@ struct BwdArgs {
 
 size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz);
 
+// side: a second stream for the key build and sort (nullptr or == stream: one stream).
 dlrm_status launch_backward(const BwdArgs& args, int dim, int index_type, void* workspace,
-                            size_t workspace_bytes, cudaStream_t stream);
+                            size_t workspace_bytes, cudaStream_t stream, cudaStream_t side);
 
 }  // namespace dlrm

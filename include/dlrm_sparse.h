@@ -162,18 +162,24 @@ dlrm_status dlrm_sparse_bwd_workspace_size(const dlrm_tables *tables,
  * grad_dense (device, B x D, written).  workspace: device, at least
  * dlrm_sparse_bwd_workspace_size() bytes, 16-byte aligned, contents ignored.
  * Ordering: the step is one operation on `stream`, after the work queued on
- * it before the call and before the work queued after.  Inside, the sort of
- * step 2 runs beside step 1 on a stream the library owns, one per device,
- * forked from `stream` and joined back to it with events.  The first call on
- * a device creates that stream; make it before any stream capture.  Host
- * threads calling at the same time are serialised while they queue work. */
+ * it before the call and before the work queued after.  side_stream is
+ * optional: NULL (or equal to stream) runs every kernel on `stream`; another
+ * stream of the same device takes the lookup-key build and the sort of
+ * step 2, which then run beside step 1.  That stream is forked from `stream`
+ * and joined back to it by two events the call creates and releases (no
+ * state outlives the call), so the caller may reuse it for anything else and
+ * the pattern holds under stream capture.  The library keeps no global
+ * state: calls on different streams are independent.
+ * Limits (DLRM_ERR_UNSUPPORTED): total rows over all tables < 2^32 - 1,
+ * T * B < 2^32, nnz < 2^32 (32-bit sort keys, values and positions). */
 dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables *tables, const dlrm_bags *bags,
                                     dlrm_pool_mode mode, const float *dense,
                                     const float *pooled_saved,
                                     const float *grad_out, float *grad_dense,
                                     float *const *accum, float lr, float eps,
                                     void *workspace, size_t workspace_bytes,
-                                    int32_t *status_dev, cudaStream_t stream);
+                                    int32_t *status_dev, cudaStream_t stream,
+                                    cudaStream_t side_stream);
 
 /* Bytes of the fixed scratch behind dlrm_sparse_bwd_adagrad_static. */
 #define DLRM_STATIC_SCRATCH_BYTES (32u << 20)
@@ -187,13 +193,15 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables *tables, const dlrm_bags *
  * DLRM_STATIC_SCRATCH_BYTES of device memory that the library holds on every
  * device that loads it, until the process exits.  Arguments, layouts and
  * results are those of dlrm_sparse_bwd_adagrad without workspace /
- * workspace_bytes.
+ * workspace_bytes and side_stream (every kernel runs on `stream`).
  *   - Returns DLRM_ERR_INVALID_ARG, before touching the GPU, when the batch
  *     needs more scratch than DLRM_STATIC_SCRATCH_BYTES
  *     (dlrm_sparse_bwd_workspace_size() says how much it needs).
- *   - The first call on a device looks up the array's device address (and
- *     so loads that part of the library onto the device); make that first
- *     call before any stream capture.
+ *   - Every call looks up the array's device address on the current device
+ *     (the first call on a device also loads that part of the library onto
+ *     it); make that first call before any stream capture.  Looking it up
+ *     each time keeps the address right after the device's context has been
+ *     reset and made again.
  *   - All calls on a device share the array: calls that overlap on the GPU
  *     (other streams, or host threads without ordering) race and must be
  *     serialised by the caller.  No scratch contents carry over between

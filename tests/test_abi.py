@@ -45,7 +45,7 @@ def test_built_for_sm103a():
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dlrm_abi_version() == 1
+    assert lib.dlrm_abi_version() == 2
     assert lib.dlrm_status_string(0) == b"ok"
     assert lib.dlrm_status_string(dl.DLRM_ERR_INDEX_OOB) == b"index out of range"
     assert lib.dlrm_status_string(dl.DLRM_ERR_INVALID_ARG | dl.DLRM_ERR_TIMEOUT) == b"invalid argument"
@@ -77,8 +77,38 @@ def test_host_argument_checks(lib):
     assert lib.dlrm_interact_fwd(0x1000, 0x2000, 4, 0, 128, 0x3000, None) == 1
     bf, _a, _b = _tables(dtype=1)
     st = lib.dlrm_sparse_bwd_adagrad(ctypes.byref(bf), ctypes.byref(bags), 0, 0x10, 0x10, 0x10, 0x10,
-                                     (ctypes.c_void_p * 2)(0x10, 0x10), 0.01, 1e-8, 0x10, 1 << 30, None, None)
+                                     (ctypes.c_void_p * 2)(0x10, 0x10), 0.01, 1e-8, 0x10, 1 << 30, None, None, None)
     assert st == dl.DLRM_ERR_UNSUPPORTED
+
+
+def _bwd_status(lib, T, B, nnz, itype=1, rows=10):
+    tb, _p, _r = _tables(T=T, D=16, rows=rows)
+    bags = dl.DlrmBags(B, nnz, itype, 0x2000, 0x3000)
+    acc = (ctypes.c_void_p * T)(*[0x10] * T)
+    return lib.dlrm_sparse_bwd_adagrad(ctypes.byref(tb), ctypes.byref(bags), 0, 0x10, 0x10, 0x10, 0x10, acc, 0.01,
+                                       1e-8, 0x10, 1 << 62, None, None, None)
+
+
+def test_backward_rejects_batches_past_32_bit_sort_fields(lib):
+    """The backward sorts 32-bit keys (global rows), values (b*T + t) and positions: T*B >= 2^32 or
+    nnz >= 2^32 is refused on the host, before any launch (int64 indices, so the forward accepts both)."""
+    assert _bwd_status(lib, T=2, B=1 << 31, nnz=8) == dl.DLRM_ERR_UNSUPPORTED      # T*B = 2^32
+    assert _bwd_status(lib, T=2, B=4, nnz=1 << 32) == dl.DLRM_ERR_UNSUPPORTED      # nnz = 2^32
+    assert _bwd_status(lib, T=1, B=4, nnz=8, rows=(1 << 32) - 1) == dl.DLRM_ERR_UNSUPPORTED  # rows
+    # just inside every limit the host checks pass and only the (huge) workspace need remains
+    n = ctypes.c_size_t(0)
+    tb, _p, _r = _tables(T=2, D=16)
+    bags = dl.DlrmBags((1 << 31) - 1, (1 << 32) - 1, 1, 0x2000, 0x3000)
+    assert lib.dlrm_sparse_bwd_workspace_size(ctypes.byref(tb), ctypes.byref(bags), ctypes.byref(n)) == 0
+    assert n.value > 1 << 36
+
+
+def test_static_scratch_size_matches_header(lib):
+    """The binding's copy of DLRM_STATIC_SCRATCH_BYTES is the header's."""
+    text = open(os.path.join(ROOT, "include", "dlrm_sparse.h")).read()
+    m = re.search(r"#define\s+DLRM_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "DLRM_STATIC_SCRATCH_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == dl.STATIC_SCRATCH_BYTES
 
 
 def test_workspace_size_grows_with_batch(lib):

@@ -8,8 +8,8 @@ import torch
 import embedding_bag_lookup_dlrm_b300 as dl
 import gen
 import oracle
-from gpu_util import (TOL_ADAGRAD, TOL_INTERACT, assert_close, batch_to_device, dev_index, dev_tables, free_cuda,
-                      random_case, workload_tables)
+from gpu_util import (TOL_ADAGRAD, TOL_INTERACT, TOL_POOL_F32, assert_close, batch_to_device, dev_index, dev_tables,
+                      free_cuda, random_case, workload_tables)
 
 pytestmark = pytest.mark.gpu
 
@@ -165,7 +165,10 @@ def test_workload_training_step(orc):
     w = gen.workload(5)
     batch, = gen.make_batches(w, [0])
     tabs_host, nr, cidx = gen.compact_tables(w, batch)
-    pooled, st = orc.embbag(tabs_host, nr, cidx, batch.offsets, w.B, w.D, w.mode)
+    fwd_ref = orc.sparse_fwd(tabs_host, nr, cidx, batch.offsets, batch.dense, w.mode, with_abs=True,
+                             with_pooled=True)
+    pooled_ref, pabs, st = orc.embbag(tabs_host, nr, cidx, batch.offsets, w.B, w.D, w.mode, with_abs=True)
+    pooled = fwd_ref["pooled"]
     new_ref = [t.copy() for t in tabs_host]
     acc_ref = [np.full(n, w.accum_init, np.float32) for n in nr]
     gd_ref, st2 = orc.sparse_bwd_adagrad(new_ref, nr, cidx, batch.offsets, batch.dense, pooled, batch.grad_out,
@@ -177,7 +180,13 @@ def test_workload_training_step(orc):
     di, do, dx = batch_to_device(batch)
     ps = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    dl.dlrm_sparse_fwd(tabs, di, do, dx, w.mode, pooled_save=ps, status=status)
+    out = dl.dlrm_sparse_fwd(tabs, di, do, dx, w.mode, pooled_save=ps, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0 and fwd_ref["status"] == 0
+    # the forward of the step (the multi-lookup tensor-core kernel), every value against the oracle
+    assert_close(out.cpu().numpy(), fwd_ref["out"], fwd_ref["out_abs"], TOL_INTERACT, "training forward out")
+    assert_close(ps.cpu().numpy(), pooled_ref, pabs, TOL_POOL_F32, "training forward pooled_save")
+    del out
     gd = dl.dlrm_sparse_bwd_adagrad(tabs, acc, di, do, dx, ps, torch.from_numpy(batch.grad_out).cuda(), w.lr,
                                     w.eps, w.mode, status=status)
     torch.cuda.synchronize()

@@ -78,6 +78,46 @@ def test_fused_embbag_interact(case, orc):
     assert_close(out2.cpu().numpy(), ref["out"], ref["out_abs"], TOL_INTERACT, "interact out")
 
 
+# More tiles than the tensor-core kernel keeps resident (148 SMs x 3 CTAs = 444), so every CTA walks
+# several tiles of its persistent loop: metadata read one and two tiles ahead, the MMA barrier's phase
+# flipping, operand buffers reused.  Bags of 1..8 (mean 4.5) take the multi-lookup variant, bags of 0..2
+# (mean 1) the one-hot variant with its row-by-row pooling of the longer bags.
+MULTI_TILE_CASES = [
+    # D, T, dtype, mode, itype, Lmin, Lmax, B, V
+    (128, 26, "f32", "sum", "i32", 1, 8, 4001, 5000),
+    (128, 26, "f32", "mean", "i64", 1, 8, 4003, 5000),
+    (128, 26, "bf16", "sum", "i64", 1, 8, 4005, 5000),
+    (128, 26, "bf16", "mean", "i32", 1, 8, 4002, 5000),
+    (128, 26, "f32", "mean", "i32", 0, 8, 4000, 300),
+    (64, 40, "f32", "sum", "i32", 1, 4, 2001, 2000),
+    (64, 40, "bf16", "mean", "i64", 0, 4, 2003, 2000),
+    (128, 26, "f32", "sum", "i32", 0, 2, 4007, 5000),
+    (128, 80, "f32", "sum", "i64", 1, 3, 501, 1000),
+]
+
+
+@pytest.mark.parametrize("case", MULTI_TILE_CASES, ids=lambda c: "D{}-T{}-{}-{}-{}-L{}..{}-B{}-V{}".format(*c))
+def test_fused_multi_tile(case, orc):
+    D, T, dtype, mode, itype, Lmin, Lmax, B, V = case
+    tabs, Vs, idx, off, dense = random_case(700 + MULTI_TILE_CASES.index(case), B, T, D, V, Lmin, Lmax, dtype)
+    ref = orc.sparse_fwd(tabs, Vs, idx, off, dense, mode, dtype, with_abs=True)
+    pooled_ref, pabs, st = orc.embbag(tabs, Vs, idx, off, B, D, mode, dtype, with_abs=True)
+    assert st == 0 and ref["status"] == 0
+    dt = dev_tables(tabs, dtype)
+    di, do = dev_index(idx, itype), dev_index(off, itype)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pooled_save = torch.empty((B, T, D), dtype=torch.float32, device="cuda")
+    out = dl.dlrm_sparse_fwd(dt, di, do, torch.from_numpy(dense).cuda(), mode, pooled_save=pooled_save,
+                             status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    o = out.cpu().numpy()
+    assert np.array_equal(o[:, :D].view(np.uint32), dense.view(np.uint32)), "dense part not copied exactly"
+    assert_close(o, ref["out"], ref["out_abs"], TOL_INTERACT if dtype == "f32" else TOL_BF16, "fused out")
+    assert_close(pooled_save.cpu().numpy(), pooled_ref, pabs, TOL_BF16 if dtype == "bf16" else TOL_POOL_F32,
+                 "fused pooled_save")
+
+
 def test_onehot_fp32_bit_exact(orc):
     B, T, D = 77, 26, 128
     tabs, Vs, idx, off, dense = random_case(5, B, T, D, 300, 1, 1)

@@ -1,7 +1,10 @@
 """A training step (dlrm_sparse_fwd with pooled_save, then dlrm_sparse_bwd_adagrad)
 captured into a CUDA graph and replayed gives, bitwise, what the same steps give
-when called directly: the backward's side stream forks from and joins the
-captured stream, and every kernel of the step is deterministic."""
+when called directly: the caller's side stream forks from and joins the
+captured stream (through events the call makes and releases), and every kernel
+of the step is deterministic.  Steps queued on independent streams at once give
+the results of the same steps run one after another: the library holds no
+state shared between calls."""
 import numpy as np
 import pytest
 import torch
@@ -15,8 +18,9 @@ pytestmark = pytest.mark.gpu
 class Step:
     """Buffers of one training step, allocated once, so that a graph can replay it."""
 
-    def __init__(self, tabs, Vs, idx, off, dense, grad_out, D):
+    def __init__(self, tabs, Vs, idx, off, dense, grad_out, D, side=None):
         B, T = dense.shape[0], len(tabs)
+        self.side = side
         self.tables = dev_tables(tabs, "f32")
         self.accum = [torch.full((v,), 0.1, device="cuda") for v in Vs]
         self.di, self.do = dev_index(idx, "i32"), dev_index(off, "i32")
@@ -33,27 +37,29 @@ class Step:
         dl.dlrm_sparse_fwd(self.tables, self.di, self.do, self.dx, out=self.out, pooled_save=self.ps,
                            status=self.status)
         dl.dlrm_sparse_bwd_adagrad(self.tables, self.accum, self.di, self.do, self.dx, self.ps, self.g, 0.01, 1e-8,
-                                   grad_dense=self.gd, workspace=self.ws, status=self.status)
+                                   grad_dense=self.gd, workspace=self.ws, status=self.status, side_stream=self.side)
 
     def state(self):
         return [t.clone() for t in self.tables] + [a.clone() for a in self.accum] + [self.out.clone(),
                                                                                       self.gd.clone()]
 
 
-def test_graph_replay_matches_direct_calls():
+@pytest.mark.parametrize("two_streams", [True, False], ids=["side-stream", "one-stream"])
+def test_graph_replay_matches_direct_calls(two_streams):
     B, T, D, V = 3000, 26, 128, 500
     tabs, Vs, idx, off, dense = random_case(77, B, T, D, V, 1, 8, value_scale=0.05)
     g = np.random.default_rng(5).standard_normal((B, D + (T + 1) * T // 2)).astype(np.float32)
+    side = torch.cuda.Stream(priority=-100) if two_streams else None
 
-    direct = Step(tabs, Vs, idx, off, dense, g, D)
-    direct.run()  # also the first call on the device: creates the library's side stream, configures kernels
+    direct = Step(tabs, Vs, idx, off, dense, g, D, side)
+    direct.run()
     torch.cuda.synchronize()
     after_one = direct.state()
     direct.run()
     torch.cuda.synchronize()
     after_two = direct.state()
 
-    graphed = Step(tabs, Vs, idx, off, dense, g, D)
+    graphed = Step(tabs, Vs, idx, off, dense, g, D, side)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         graphed.run()
@@ -72,10 +78,11 @@ def test_graph_replay_matches_direct_calls():
     assert direct.status.item() == 0 and graphed.status.item() == 0
 
 
-def test_step_on_another_stream_matches_default_stream():
+@pytest.mark.parametrize("two_streams", [True, False], ids=["side-stream", "one-stream"])
+def test_step_on_another_stream_matches_default_stream(two_streams):
     """The step called on a non-default stream gives the default stream's results, and work queued on
     that stream right after the call (copies of the updated state, no synchronisation in between)
-    already sees them: the library's side stream joins the caller's stream before the call returns."""
+    already sees them: the side stream joins the caller's stream before the call returns."""
     B, T, D, V = 2000, 26, 128, 300
     tabs, Vs, idx, off, dense = random_case(78, B, T, D, V, 1, 8, value_scale=0.05)
     g = np.random.default_rng(6).standard_normal((B, D + (T + 1) * T // 2)).astype(np.float32)
@@ -84,7 +91,7 @@ def test_step_on_another_stream_matches_default_stream():
     torch.cuda.synchronize()
     expected = ref.state()
 
-    step = Step(tabs, Vs, idx, off, dense, g, D)
+    step = Step(tabs, Vs, idx, off, dense, g, D, torch.cuda.Stream() if two_streams else None)
     other = torch.cuda.Stream()
     other.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(other):
@@ -93,3 +100,31 @@ def test_step_on_another_stream_matches_default_stream():
     torch.cuda.synchronize()
     for a, b in zip(snap, expected):
         assert torch.equal(a, b)
+
+
+def test_independent_streams_run_at_once():
+    """Two steps on their own tables, queued together on two streams (each with its own side stream),
+    give what each gives alone."""
+    B, T, D, V = 2500, 26, 128, 400
+    cases = []
+    for k in range(2):
+        tabs, Vs, idx, off, dense = random_case(90 + k, B, T, D, V, 1, 8, value_scale=0.05)
+        g = np.random.default_rng(20 + k).standard_normal((B, D + (T + 1) * T // 2)).astype(np.float32)
+        cases.append((tabs, Vs, idx, off, dense, g))
+    expected = []
+    for c in cases:
+        alone = Step(*c, D)
+        alone.run()
+        torch.cuda.synchronize()
+        expected.append(alone.state())
+    steps = [Step(*c, D, torch.cuda.Stream()) for c in cases]
+    streams = [torch.cuda.Stream() for _ in cases]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    for step, st in zip(steps, streams):
+        with torch.cuda.stream(st):
+            step.run()
+    torch.cuda.synchronize()
+    for step, exp in zip(steps, expected):
+        for a, b in zip(step.state(), exp):
+            assert torch.equal(a, b)

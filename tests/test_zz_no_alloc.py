@@ -77,14 +77,59 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 
 
 def test_static_scratch_rejects_a_batch_too_large():
-    """A batch whose scratch exceeds the fixed array is refused before any launch."""
+    """A batch whose scratch exceeds the fixed array is refused before any launch, and it is the size
+    that refuses it: the same arguments pass every other host check (the workspace query accepts them
+    and reports a need above the array's size)."""
     lib = dl.load_library()
     B, nnz = 1 << 16, 1 << 20   # dP alone is B*T*D*4 = 872 MB
     ptrs = (ctypes.c_void_p * T)(*[0x1000] * T)
     rows = (ctypes.c_int64 * T)(*[V] * T)
     tb = dl.DlrmTables(T, D, 0, ptrs, rows)
     bags = dl.DlrmBags(B, nnz, 0, 0x2000, 0x3000)
+    need = ctypes.c_size_t(0)
+    assert lib.dlrm_sparse_bwd_workspace_size(ctypes.byref(tb), ctypes.byref(bags), ctypes.byref(need)) == 0
+    assert need.value > dl.STATIC_SCRATCH_BYTES
     acc = (ctypes.c_void_p * T)(*[0x4000] * T)
     st = lib.dlrm_sparse_bwd_adagrad_static(ctypes.byref(tb), ctypes.byref(bags), 0, 0x5000, 0x6000, 0x7000,
                                             0x8000, acc, 0.01, 1e-8, None, None)
     assert st == dl.DLRM_ERR_INVALID_ARG
+
+
+def test_static_scratch_accepts_a_batch_just_under_the_limit():
+    """The largest batch (bags of 1..8) whose scratch fits the fixed array runs, and matches the
+    workspace entry point; one more sample no longer fits."""
+    rng = np.random.default_rng(601)
+    Bmax = 4000
+    L = rng.integers(1, 9, size=(T, Bmax))
+    tb = dl.Tables([torch.empty((V, D), dtype=torch.float32, device="cuda") for _ in range(1)] * T)
+
+    def need(B):
+        off = np.zeros(T * B + 1, np.int32)
+        np.cumsum(L[:, :B].reshape(-1), out=off[1:])
+        idx = np.zeros(int(off[-1]), np.int32)
+        return dl.dlrm_sparse_bwd_workspace_size(tb, torch.from_numpy(idx), torch.from_numpy(off))
+
+    lo, hi = 1, Bmax   # need(lo) fits, need(hi) does not
+    assert need(hi) > dl.STATIC_SCRATCH_BYTES
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if need(mid) <= dl.STATIC_SCRATCH_BYTES else (lo, mid)
+    B = lo
+    assert dl.STATIC_SCRATCH_BYTES - need(B) < 64 << 10   # within 64 KB of the limit
+
+    tabs = [rng.uniform(-0.05, 0.05, size=(V, D)).astype(np.float32) for _ in range(T)]
+    off = np.zeros(T * B + 1, np.int64)
+    np.cumsum(L[:, :B].reshape(-1), out=off[1:])
+    idx = rng.integers(0, V, size=int(off[-1]))
+    dense = rng.standard_normal((B, D)).astype(np.float32)
+    g = rng.standard_normal((B, D + (T + 1) * T // 2)).astype(np.float32)
+    batch = (tabs, [V] * T, idx, off, dense, g)
+    ref_t, ref_a = _state(tabs, [V] * T)
+    ref_gd = _step(dl.dlrm_sparse_bwd_adagrad, ref_t, ref_a, batch)
+    got_t, got_a = _state(tabs, [V] * T)
+    got_gd = _step(dl.dlrm_sparse_bwd_adagrad_static, got_t, got_a, batch,
+                   grad_dense=torch.empty((B, D), dtype=torch.float32, device="cuda"))
+    assert_close(got_gd, ref_gd, np.abs(ref_gd) + 1e-6, TOL_INTERACT, "grad_dense at the size limit")
+    for t in range(T):
+        scale = np.abs(tabs[t]) + np.abs(tabs[t] - ref_t[t].cpu().numpy())
+        assert_close(got_t[t].cpu().numpy(), ref_t[t].cpu().numpy(), scale, TOL_ADAGRAD, f"rows of table {t}")
