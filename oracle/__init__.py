@@ -24,6 +24,7 @@ INDEX_OOB = 2
 BAD_OFFSETS = 4
 MODES = {"sum": 0, "mean": 1}
 DTYPES = {"f32": 0, "bf16": 1}
+RULES = {"adagrad": 0, "sgd": 1}
 
 
 def build(src: str = SRC, out: str = LIB, extra_flags=()) -> str:
@@ -57,6 +58,14 @@ class Oracle:
         lib.oracle_sparse_bwd_adagrad.argtypes = [_I, _I, _P, _P, _I64, _I64, _P, _P, _I, _P, _P, _P, _P,
                                                   _P, ctypes.c_float, ctypes.c_float]
         lib.oracle_sparse_bwd_adagrad.restype = _I
+        lib.oracle_sparse_bwd_update.argtypes = [_I, _I, _P, _P, _I64, _I64, _P, _P, _I, _P, _P, _P, _P, _I,
+                                                 _P, ctypes.c_float, ctypes.c_float]
+        lib.oracle_sparse_bwd_update.restype = _I
+        lib.oracle_embbag_bwd_update.argtypes = [_I, _I, _P, _P, _I64, _I64, _P, _P, _I, _P, _I, _P,
+                                                 ctypes.c_float, ctypes.c_float]
+        lib.oracle_embbag_bwd_update.restype = _I
+        lib.oracle_hash_indices.argtypes = [_I, _I64, _I64, _P, _P, _P, _P]
+        lib.oracle_hash_indices.restype = _I
         self.lib = lib
 
     # -- helpers ---------------------------------------------------------
@@ -151,6 +160,57 @@ class Oracle:
                                                 pooled.ctypes.data, grad_out.ctypes.data, gd.ctypes.data,
                                                 aptr, ctypes.c_float(lr), ctypes.c_float(eps))
         return gd, st
+
+
+    def sparse_bwd_update(self, tables, num_rows, indices, offsets, dense, pooled, grad_out, rule, lr, eps=0.0,
+                          accum=None, mode="sum"):
+        """The training step with update rule "adagrad" (needs accum) or "sgd"; tables (and accum) are
+        updated in place; returns (grad_dense, status)."""
+        dense = np.ascontiguousarray(dense, dtype=np.float32)
+        pooled = np.ascontiguousarray(pooled, dtype=np.float32)
+        grad_out = np.ascontiguousarray(grad_out, dtype=np.float32)
+        B, T, D = pooled.shape
+        tptr, aptr = self._rows_and_accum(tables, accum, rule, T)
+        nr, idx, off = self._csr(num_rows, indices, offsets)
+        gd = np.empty((B, D), dtype=np.float32)
+        st = self.lib.oracle_sparse_bwd_update(T, D, tptr, nr.ctypes.data, B, idx.size, idx.ctypes.data,
+                                               off.ctypes.data, MODES[mode], dense.ctypes.data, pooled.ctypes.data,
+                                               grad_out.ctypes.data, gd.ctypes.data, RULES[rule], aptr,
+                                               ctypes.c_float(lr), ctypes.c_float(eps))
+        return gd, st
+
+    def embbag_bwd_update(self, tables, num_rows, indices, offsets, grad_pooled, rule, lr, eps=0.0, accum=None,
+                          mode="sum"):
+        """Per-row gradient sums from grad_pooled [B, T, D] and one update of each touched row (in place);
+        returns the status."""
+        grad_pooled = np.ascontiguousarray(grad_pooled, dtype=np.float32)
+        B, T, D = grad_pooled.shape
+        tptr, aptr = self._rows_and_accum(tables, accum, rule, T)
+        nr, idx, off = self._csr(num_rows, indices, offsets)
+        return self.lib.oracle_embbag_bwd_update(T, D, tptr, nr.ctypes.data, B, idx.size, idx.ctypes.data,
+                                                 off.ctypes.data, MODES[mode], grad_pooled.ctypes.data,
+                                                 RULES[rule], aptr, ctypes.c_float(lr), ctypes.c_float(eps))
+
+    def hash_indices(self, num_rows, raw_ids, offsets, B):
+        """rows[p] = raw_ids[p] (unsigned 64-bit) mod V_t of the table holding position p; (rows, status)."""
+        raw = np.ascontiguousarray(raw_ids).view(np.uint64) if np.asarray(raw_ids).dtype in (np.int64, np.uint64) \
+            else np.ascontiguousarray(raw_ids, dtype=np.uint64)
+        nr = np.ascontiguousarray(num_rows, dtype=np.int64)
+        off = np.ascontiguousarray(offsets, dtype=np.int64)
+        rows = np.empty(raw.size, dtype=np.int64)
+        st = self.lib.oracle_hash_indices(nr.size, B, raw.size, nr.ctypes.data, raw.ctypes.data, off.ctypes.data,
+                                          rows.ctypes.data)
+        return rows, st
+
+    @staticmethod
+    def _rows_and_accum(tables, accum, rule, T):
+        for a in list(tables) + list(accum or []):
+            assert a.dtype == np.float32 and a.flags.c_contiguous
+        if rule == "adagrad":
+            assert accum is not None and len(accum) == T
+        tptr = (ctypes.c_void_p * T)(*[t.ctypes.data for t in tables])
+        aptr = (ctypes.c_void_p * T)(*[a.ctypes.data for a in accum]) if accum is not None else None
+        return tptr, aptr
 
 
 _default = None

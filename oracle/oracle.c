@@ -44,6 +44,12 @@
  *     w_d -= lr * g_d / (sqrt(A) + eps); the gradients of all lookups of a row
  *     in one step are summed first (one update per touched row); rows not
  *     touched are left alone.
+ *   - plain SGD (the other rule the same sentence names) is w_d -= lr * g_d on
+ *     the same per-row gradient sums: no momentum, no weight decay;
+ *   - the hashing of raw feature IDs into a table of V_t rows ("Deep Learning
+ *     Recommendation Model (DLRM)", notes.helloworld.co.in, "Why it is mostly
+ *     a systems problem") is read as the plainest hash: the ID, taken as an
+ *     unsigned 64-bit integer, modulo V_t.
  */
 #include <math.h>
 #include <stddef.h>
@@ -60,6 +66,9 @@
 
 #define ORACLE_SUM 0
 #define ORACLE_MEAN 1
+
+#define ORACLE_ADAGRAD 0
+#define ORACLE_SGD 1
 
 /* One table element widened to double.  bf16 is the top half of an fp32
  * pattern, so widening is exact. */
@@ -284,30 +293,23 @@ static int cmp_lookup(const void *a, const void *b)
     return x->b < y->b ? -1 : (x->b > y->b);
 }
 
-/* One training step of the sparse path (fp32 tables only):
- *   1. dV from oracle_interact_bwd, in double; grad_dense receives dx;
- *   2. per table t, every valid lookup p of bag (t,b) contributes
- *      dP[b][t] * (mean ? 1/L : 1) to its row; the lookups of a row are
- *      visited in original position order (sorted by (row, position));
- *   3. per touched row r:  A_r += sum_d g_d^2 / D;
- *                          w_r,d -= lr * g_d / (sqrt(A_r) + eps),
- *      in double, rounded once to float.
- * tables[] and accum[] are updated in place.  Returns the status bits.
- * When the offsets are malformed only the status is meaningful. */
-int oracle_sparse_bwd_adagrad(int T, int D, float *const *tables,
-                              const int64_t *num_rows, int64_t B, int64_t nnz,
-                              const int64_t *indices, const int64_t *offsets,
-                              int mode, const float *dense, const float *pooled,
-                              const float *grad_out, float *grad_dense,
-                              float *const *accum, float lr, float eps)
+/* Steps 2-3 of the training step, per table t:  every valid lookup p of bag
+ * (t,b) contributes grad(b,t) * (mean ? 1/L : 1) to its row, the lookups of a
+ * row visited in original position order (sorted by (row, position)); then
+ * one update of each touched row r with its gradient sum g:
+ *   ADAGRAD:  A_r += sum_d g_d^2 / D;  w_r,d -= lr * g_d / (sqrt(A_r) + eps)
+ *   SGD:      w_r,d -= lr * g_d
+ * in double, rounded once to float.  grad(b,t) is the D doubles at
+ * grad + b * grad_stride_b + (t + grad_t0) * D.  Returns the status bits. */
+static int update_rows(int T, int D, float *const *tables,
+                       const int64_t *num_rows, int64_t B, int64_t nnz,
+                       const int64_t *indices, const int64_t *offsets, int mode,
+                       const double *grad, int64_t grad_stride_b, int grad_t0,
+                       int rule, float *const *accum, float lr, float eps)
 {
-    const int N = T + 1;
     int status = ORACLE_OK;
     if (offsets[0] != 0 || offsets[(int64_t)T * B] != nnz)
         status |= ORACLE_BAD_OFFSETS;
-
-    double *dV = malloc(sizeof(double) * (size_t)B * N * D);
-    oracle_interact_bwd(B, T, D, dense, pooled, grad_out, grad_dense, NULL, dV);
 
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
     for (int t = 0; t < T; ++t) {
@@ -345,25 +347,112 @@ int oracle_sparse_bwd_adagrad(int T, int D, float *const *tables,
                 g[d] = 0.0;
             for (; e < n && refs[e].row == refs[s].row; ++e) {
                 double scale = (mode == ORACLE_MEAN) ? 1.0 / (double)refs[e].L : 1.0;
-                const double *dp = dV + ((size_t)refs[e].b * N + (t + 1)) * D;
+                const double *dp = grad + (size_t)refs[e].b * grad_stride_b + (size_t)(t + grad_t0) * D;
                 for (int d = 0; d < D; ++d)
                     g[d] += dp[d] * scale;
             }
             int64_t r = refs[s].row;
-            double ss = 0.0;
-            for (int d = 0; d < D; ++d)
-                ss += g[d] * g[d];
-            double A = (double)accum[t][r] + ss / (double)D;
-            double den = sqrt(A) + (double)eps;
             float *w = tables[t] + r * (int64_t)D;
-            for (int d = 0; d < D; ++d)
-                w[d] = (float)((double)w[d] - (double)lr * g[d] / den);
-            accum[t][r] = (float)A;
+            if (rule == ORACLE_SGD) {
+                for (int d = 0; d < D; ++d)
+                    w[d] = (float)((double)w[d] - (double)lr * g[d]);
+            } else {
+                double ss = 0.0;
+                for (int d = 0; d < D; ++d)
+                    ss += g[d] * g[d];
+                double A = (double)accum[t][r] + ss / (double)D;
+                double den = sqrt(A) + (double)eps;
+                for (int d = 0; d < D; ++d)
+                    w[d] = (float)((double)w[d] - (double)lr * g[d] / den);
+                accum[t][r] = (float)A;
+            }
             s = e;
         }
         free(g);
         free(refs);
     }
+    return status;
+}
+
+/* One training step of the sparse path (fp32 tables only):
+ *   1. dV from oracle_interact_bwd, in double; grad_dense receives dx;
+ *   2-3. update_rows with dP_t = dV_{t+1} and the given rule.
+ * tables[] and accum[] (Adagrad only) are updated in place.  Returns the
+ * status bits.  When the offsets are malformed only the status is
+ * meaningful. */
+int oracle_sparse_bwd_update(int T, int D, float *const *tables,
+                             const int64_t *num_rows, int64_t B, int64_t nnz,
+                             const int64_t *indices, const int64_t *offsets,
+                             int mode, const float *dense, const float *pooled,
+                             const float *grad_out, float *grad_dense, int rule,
+                             float *const *accum, float lr, float eps)
+{
+    const int N = T + 1;
+    double *dV = malloc(sizeof(double) * (size_t)B * N * D);
+    oracle_interact_bwd(B, T, D, dense, pooled, grad_out, grad_dense, NULL, dV);
+    int status = update_rows(T, D, tables, num_rows, B, nnz, indices, offsets, mode,
+                             dV, (int64_t)N * D, 1, rule, accum, lr, eps);
     free(dV);
+    return status;
+}
+
+/* The Adagrad training step ("DLRM", robocikowo.com, "Forward pass", last
+ * sentence, with the row-wise reading). */
+int oracle_sparse_bwd_adagrad(int T, int D, float *const *tables,
+                              const int64_t *num_rows, int64_t B, int64_t nnz,
+                              const int64_t *indices, const int64_t *offsets,
+                              int mode, const float *dense, const float *pooled,
+                              const float *grad_out, float *grad_dense,
+                              float *const *accum, float lr, float eps)
+{
+    return oracle_sparse_bwd_update(T, D, tables, num_rows, B, nnz, indices, offsets, mode,
+                                    dense, pooled, grad_out, grad_dense, ORACLE_ADAGRAD,
+                                    accum, lr, eps);
+}
+
+/* Steps 2-3 alone, from a given gradient of the pooled vectors
+ * grad_pooled[B][T][D] (float, as the interaction backward writes it). */
+int oracle_embbag_bwd_update(int T, int D, float *const *tables,
+                             const int64_t *num_rows, int64_t B, int64_t nnz,
+                             const int64_t *indices, const int64_t *offsets,
+                             int mode, const float *grad_pooled, int rule,
+                             float *const *accum, float lr, float eps)
+{
+    double *g = malloc(sizeof(double) * ((size_t)B * T * D + 1));
+    for (size_t i = 0; i < (size_t)B * T * D; ++i)
+        g[i] = (double)grad_pooled[i];
+    int status = update_rows(T, D, tables, num_rows, B, nnz, indices, offsets, mode,
+                             g, (int64_t)T * D, 0, rule, accum, lr, eps);
+    free(g);
+    return status;
+}
+
+/* Raw feature IDs to rows of their tables: rows[p] = raw[p] mod V_t, the ID
+ * read as an unsigned 64-bit integer, t the table whose bags hold position p
+ * (table-major offsets: t with offsets[t*B] <= p < offsets[(t+1)*B]).
+ * Positions outside every table's range (malformed offsets) get row 0 and
+ * raise ORACLE_BAD_OFFSETS.  Returns the status bits. */
+int oracle_hash_indices(int T, int64_t B, int64_t nnz, const int64_t *num_rows,
+                        const uint64_t *raw, const int64_t *offsets, int64_t *rows)
+{
+    int status = ORACLE_OK;
+    if (offsets[0] != 0 || offsets[(int64_t)T * B] != nnz)
+        status |= ORACLE_BAD_OFFSETS;
+    for (int64_t p = 0; p < nnz; ++p)
+        rows[p] = -1;
+    for (int t = 0; t < T; ++t) {
+        int64_t lo = offsets[(int64_t)t * B], hi = offsets[(int64_t)(t + 1) * B];
+        if (lo < 0 || hi < lo || hi > nnz) {
+            status |= ORACLE_BAD_OFFSETS;
+            continue;
+        }
+        for (int64_t p = lo; p < hi; ++p)
+            rows[p] = (int64_t)(raw[p] % (uint64_t)num_rows[t]);
+    }
+    for (int64_t p = 0; p < nnz; ++p)
+        if (rows[p] < 0) {
+            rows[p] = 0;
+            status |= ORACLE_BAD_OFFSETS;
+        }
     return status;
 }

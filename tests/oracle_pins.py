@@ -432,10 +432,99 @@ def pin_duplicates_one_update(orc):
     close(acc[0][1], A2, 0.1, 1e-6, "dup acc")
 
 
+def _table_grads(tables, idx, off, B, mode, grad_pooled):
+    """float64 autograd: d<grad_pooled, pooled(W)>/dW per table (sums over every lookup of a row)."""
+    T = len(tables)
+    Ws = [torch.from_numpy(t.astype(np.float64)).requires_grad_() for t in tables]
+    pools = []
+    for t in range(T):
+        lo = off[t * B]
+        seg = torch.from_numpy(np.asarray(idx[off[t * B]:off[(t + 1) * B]], dtype=np.int64))
+        offs = torch.from_numpy(np.asarray(off[t * B:(t + 1) * B] - lo, dtype=np.int64))
+        pools.append(F.embedding_bag(seg, Ws[t], offs, mode=mode))
+    (torch.stack(pools, 1) * torch.from_numpy(np.asarray(grad_pooled, np.float64))).sum().backward()
+    return [w.grad.numpy() for w in Ws]
+
+
+def pin_sgd_vs_autograd(orc):
+    """Plain SGD on the embedding rows, w' = w - lr * dL/dw, with dL/dw from float64 autograd of
+    <g, out> through embedding_bag and the interaction; untouched rows unchanged."""
+    for seed, mode in [(80, "sum"), (81, "mean")]:
+        tables, V, idx, off, dense = rand_problem(seed, B=7, T=3, D=6, V=(4, 3, 6), Lmax=5)
+        B, T, D = 7, 3, 6
+        pooled, _ = orc.embbag(tables, V, idx, off, B, D, mode)
+        N = T + 1
+        g = np.random.default_rng(seed + 1).standard_normal((B, D + N * (N - 1) // 2)).astype(np.float32)
+        new = [t.copy() for t in tables]
+        lr = 0.25
+        gd, st = orc.sparse_bwd_update(new, V, idx, off, dense, pooled, g, "sgd", lr, mode=mode)
+        assert st == 0
+        Pt = torch.from_numpy(pooled.astype(np.float64)).requires_grad_()
+        (torch_interact(torch.from_numpy(dense.astype(np.float64)), Pt) * torch.from_numpy(g.astype(np.float64))
+         ).sum().backward()
+        G = _table_grads(tables, idx, off, B, mode, Pt.grad.numpy())
+        for t in range(T):
+            want = (tables[t].astype(np.float64) - lr * G[t]).astype(np.float32)
+            close(new[t], want, np.abs(tables[t]) + 1e-3, 1e-6, f"sgd table {t} {mode}")
+            touched = set(idx[off[t * B]:off[(t + 1) * B]].tolist())
+            for r in range(V[t]):
+                if r not in touched:
+                    assert np.array_equal(new[t][r], tables[t][r])
+
+
+def pin_embbag_bwd_vs_autograd(orc):
+    """The row update from a given gradient of the pooled vectors: per-row gradient from float64
+    autograd through embedding_bag, then the Adagrad and the SGD closed forms."""
+    for seed, mode in [(82, "sum"), (83, "mean")]:
+        tables, V, idx, off, _ = rand_problem(seed, B=9, T=3, D=5, V=(6, 2, 5), Lmax=4)
+        B, T, D = 9, 3, 5
+        rng = np.random.default_rng(seed + 7)
+        gp = rng.standard_normal((B, T, D)).astype(np.float32)
+        G = _table_grads(tables, idx, off, B, mode, gp)
+        acc0 = [rng.uniform(0.05, 0.2, size=v).astype(np.float32) for v in V]
+        new_a, acc = [t.copy() for t in tables], [a.copy() for a in acc0]
+        assert orc.embbag_bwd_update(new_a, V, idx, off, gp, "adagrad", 0.1, 0.2, acc, mode) == 0
+        new_s = [t.copy() for t in tables]
+        assert orc.embbag_bwd_update(new_s, V, idx, off, gp, "sgd", 0.1, mode=mode) == 0
+        for t in range(T):
+            touched = set(idx[off[t * B]:off[(t + 1) * B]].tolist())
+            for r in range(V[t]):
+                if r in touched:
+                    w2, A2 = _adagrad_closed(tables[t][r], acc0[t][r], G[t][r], 0.1, 0.2)
+                    close(new_a[t][r], w2, np.abs(tables[t][r]) + 1e-3, 1e-6, f"adagrad row {t},{r}")
+                    close(acc[t][r], A2, acc0[t][r], 1e-6, f"adagrad acc {t},{r}")
+                    close(new_s[t][r], (tables[t][r] - 0.1 * G[t][r]).astype(np.float32),
+                          np.abs(tables[t][r]) + 1e-3, 1e-6, f"sgd row {t},{r}")
+                else:
+                    assert np.array_equal(new_a[t][r], tables[t][r]) and acc[t][r] == acc0[t][r]
+                    assert np.array_equal(new_s[t][r], tables[t][r])
+
+
+def pin_hash_brute_force(orc):
+    """rows = raw ID mod V_t with Python's unbounded integers, the ID as an unsigned 64-bit value (IDs
+    at and above 2^63 included), each position hashed with the row count of the table holding it."""
+    rng = np.random.default_rng(90)
+    V = [1, 7, 1 << 20, 4_294_967_311, (1 << 62) + 3]
+    B = 5
+    L = rng.integers(0, 6, size=len(V) * B)
+    off = np.zeros(len(V) * B + 1, np.int64)
+    np.cumsum(L, out=off[1:])
+    raw = rng.integers(0, 1 << 63, size=int(off[-1]), dtype=np.uint64) * np.uint64(2) + \
+        rng.integers(0, 2, size=int(off[-1]), dtype=np.uint64)
+    raw[:3] = [0, (1 << 64) - 1, 1 << 63]
+    rows, st = orc.hash_indices(V, raw, off, B)
+    assert st == 0
+    for t in range(len(V)):
+        for p in range(off[t * B], off[(t + 1) * B]):
+            assert rows[p] == int(raw[p]) % V[t], (t, p, int(raw[p]), rows[p])
+    assert all(0 <= rows[p] for p in range(rows.size))
+
+
 ALL_PINS = [
     pin_output_length, pin_onehot_bit_exact, pin_k_copies, pin_identity_tables,
     pin_pool_vs_embedding_bag, pin_empty_and_bad_inputs, pin_interact_vs_bmm,
     pin_n2_closed_form, pin_orthogonal_zero, pin_permutation_symmetry, pin_cauchy_schwarz,
     pin_bwd_vs_autograd, pin_bwd_finite_differences, pin_bwd_n2_closed_form,
     pin_adagrad_single_row, pin_row_grads_vs_autograd, pin_duplicates_one_update,
+    pin_sgd_vs_autograd, pin_embbag_bwd_vs_autograd, pin_hash_brute_force,
 ]

@@ -37,6 +37,15 @@ MUTANTS = {
     "adagrad uses old accumulator": [("double den = sqrt(A) + (double)eps;", "double den = sqrt((double)accum[t][r]) + (double)eps;")],
     "duplicates updated one by one": [("for (; e < n && refs[e].row == refs[s].row; ++e) {", "for (; e < n && e == s; ++e) {")],
     "bwd mean scale dropped": [("1.0 / (double)refs[e].L : 1.0;", "1.0 : 1.0;")],
+    "sgd adds the gradient": [("w[d] = (float)((double)w[d] - (double)lr * g[d]);",
+                               "w[d] = (float)((double)w[d] + (double)lr * g[d]);")],
+    "sgd keeps the adagrad scale": [("w[d] = (float)((double)w[d] - (double)lr * g[d]);",
+                                     "w[d] = (float)((double)w[d] - (double)lr * g[d] / (1.0 + sqrt(0.1)));")],
+    "pooled gradient read from the wrong table": [("(size_t)(t + grad_t0) * D;", "(size_t)(T - 1 - t + grad_t0) * D;")],
+    "hash as signed 64-bit": [("rows[p] = (int64_t)(raw[p] % (uint64_t)num_rows[t]);",
+                               "rows[p] = (int64_t)raw[p] % num_rows[t];")],
+    "hash with the next table's rows": [("rows[p] = (int64_t)(raw[p] % (uint64_t)num_rows[t]);",
+                                         "rows[p] = (int64_t)(raw[p] % (uint64_t)num_rows[(t + 1) % T]);")],
     "oob lookup not counted": [("int64_t L = hi - lo;\n            int started = 0;",
                                 "int64_t L = 0;\n            for (int64_t q = lo; q < hi; ++q) L += (indices[q] >= 0 && indices[q] < num_rows[t]);\n            int started = 0;")],
 }
