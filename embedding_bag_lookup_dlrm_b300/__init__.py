@@ -33,8 +33,11 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 _ITYPES = {torch.int32: 0, torch.int64: 1}
 
 C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sparse_fwd_host",
-             "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_adagrad_static",
-             "dlrm_status_string", "dlrm_abi_version")
+             "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_update",
+             "dlrm_interact_bwd", "dlrm_embbag_bwd_workspace_size", "dlrm_embbag_bwd_update", "dlrm_hash_indices",
+             "dlrm_pooled_exchange",
+             "dlrm_sparse_bwd_adagrad_static", "dlrm_status_string", "dlrm_abi_version")
+_RULES = {"adagrad": 0, "sgd": 1}
 
 
 class DlrmTables(ctypes.Structure):
@@ -45,6 +48,11 @@ class DlrmTables(ctypes.Structure):
 class DlrmBags(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("nnz", ctypes.c_int64), ("index_type", ctypes.c_int32),
                 ("indices", ctypes.c_void_p), ("offsets", ctypes.c_void_p)]
+
+
+class DlrmUpdate(ctypes.Structure):
+    _fields_ = [("rule", ctypes.c_int32), ("lr", ctypes.c_float), ("eps", ctypes.c_float),
+                ("accum", ctypes.POINTER(ctypes.c_void_p))]
 
 
 class DlrmError(RuntimeError):
@@ -75,6 +83,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dlrm_sparse_bwd_workspace_size": ([T, B, ctypes.POINTER(ctypes.c_size_t)], i32),
         "dlrm_sparse_bwd_adagrad": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p), ctypes.c_float,
                                      ctypes.c_float, P, ctypes.c_size_t, P, P, P], i32),
+        "dlrm_sparse_bwd_update": ([T, B, i32, P, P, P, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P,
+                                    P], i32),
+        "dlrm_interact_bwd": ([P, P, P, i64, i32, i32, P, P, P], i32),
+        "dlrm_embbag_bwd_workspace_size": ([T, B, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
+        "dlrm_embbag_bwd_update": ([T, B, i32, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P, P], i32),
+        "dlrm_hash_indices": ([ctypes.POINTER(ctypes.c_int64), i32, i64, i64, P, P, i32, P, P, P], i32),
+        "dlrm_pooled_exchange": ([P, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), i32, P], i32),
         "dlrm_sparse_bwd_adagrad_static": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p),
                                             ctypes.c_float, ctypes.c_float, P, P], i32),
         "dlrm_status_string": ([i32], ctypes.c_char_p),
@@ -350,3 +365,130 @@ def dlrm_sparse_bwd_adagrad_static(tables, accum, indices, offsets, dense, poole
                                                 _stream_ptr(stream, dev))
     _raise(st, "dlrm_sparse_bwd_adagrad_static")
     return grad_dense
+
+
+def _update(tb, rule, lr, eps, accum):
+    """The C update block (and the pointer array it refers to, kept alive by the caller)."""
+    if rule not in _RULES:
+        raise ValueError(f"unknown update rule {rule!r}")
+    ptrs = None
+    if rule == "adagrad":
+        if accum is None or len(accum) != tb.T:
+            raise ValueError("Adagrad needs one accumulator per table")
+        for i, a in enumerate(accum):
+            _check_cuda(a, f"accum[{i}]", torch.float32)
+            if a.numel() != tb.tensors[i].shape[0]:
+                raise ValueError(f"accum[{i}] must hold one value per row")
+        ptrs = (ctypes.c_void_p * tb.T)(*[a.data_ptr() for a in accum])
+    return DlrmUpdate(_RULES[rule], float(lr), float(eps), ptrs), ptrs
+
+
+def dlrm_sparse_bwd_update(tables, indices, offsets, dense, pooled_saved, grad_out, rule, lr, eps=0.0, accum=None,
+                           mode="sum", grad_dense=None, workspace=None, status=None, stream=None, side_stream=None):
+    """The training step with update rule "adagrad" (accum required) or "sgd"; tables (and accum)
+    are updated in place.  Returns grad_dense [B, D]."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    for name, t in (("dense", dense), ("pooled_saved", pooled_saved), ("grad_out", grad_out)):
+        _check_cuda(t, name, torch.float32)
+    upd, _keep = _update(tb, rule, lr, eps, accum)
+    if grad_dense is None:
+        grad_dense = torch.empty((B, tb.D), dtype=torch.float32, device=dense.device)
+    _check_cuda(grad_dense, "grad_dense", torch.float32)
+    if workspace is None:
+        workspace = torch.empty(max(dlrm_sparse_bwd_workspace_size(tb, indices, offsets), 16), dtype=torch.uint8,
+                                device=dense.device)
+    _check_cuda(workspace, "workspace")
+    bags = _bags(indices, offsets, B)
+    dev = _device(*tb.tensors, *(accum or []), indices, offsets, dense, pooled_saved, grad_out, grad_dense,
+                  workspace, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_bwd_update(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], dense.data_ptr(),
+                                        pooled_saved.data_ptr(), grad_out.data_ptr(), grad_dense.data_ptr(),
+                                        ctypes.byref(upd), workspace.data_ptr(), workspace.numel(),
+                                        status.data_ptr() if status is not None else None, _stream_ptr(stream, dev),
+                                        side_stream.cuda_stream if side_stream is not None else None)
+    _raise(st, "dlrm_sparse_bwd_update")
+    return grad_dense
+
+
+def dlrm_interact_bwd(dense, pooled, grad_out, grad_dense=None, grad_pooled=None, stream=None):
+    """The interaction backward alone: (grad_dense [B, D], grad_pooled [B, T, D]); no bag lengths applied."""
+    lib = load_library()
+    for name, t in (("dense", dense), ("pooled", pooled), ("grad_out", grad_out)):
+        _check_cuda(t, name, torch.float32)
+    B, T, D = pooled.shape
+    if grad_dense is None:
+        grad_dense = torch.empty((B, D), dtype=torch.float32, device=dense.device)
+    if grad_pooled is None:
+        grad_pooled = torch.empty((B, T, D), dtype=torch.float32, device=dense.device)
+    _check_cuda(grad_dense, "grad_dense", torch.float32)
+    _check_cuda(grad_pooled, "grad_pooled", torch.float32)
+    dev = _device(dense, pooled, grad_out, grad_dense, grad_pooled)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_interact_bwd(dense.data_ptr(), pooled.data_ptr(), grad_out.data_ptr(), B, T, D,
+                                   grad_dense.data_ptr(), grad_pooled.data_ptr(), _stream_ptr(stream, dev))
+    _raise(st, "dlrm_interact_bwd")
+    return grad_dense, grad_pooled
+
+
+def dlrm_embbag_bwd_workspace_size(tables, indices, offsets, mode="sum") -> int:
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    bags = _bags(indices, offsets, B, device=False)
+    n = ctypes.c_size_t(0)
+    _raise(lib.dlrm_embbag_bwd_workspace_size(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], ctypes.byref(n)),
+           "dlrm_embbag_bwd_workspace_size")
+    return int(n.value)
+
+
+def dlrm_embbag_bwd_update(tables, indices, offsets, grad_pooled, rule, lr, eps=0.0, accum=None, mode="sum",
+                           workspace=None, status=None, stream=None, side_stream=None):
+    """Per-row gradient sums from grad_pooled [B, T, D] and one update of every touched row, in place."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    _check_cuda(grad_pooled, "grad_pooled", torch.float32)
+    if tuple(grad_pooled.shape) != (B, tb.T, tb.D):
+        raise ValueError(f"grad_pooled must be [{B}, {tb.T}, {tb.D}]")
+    upd, _keep = _update(tb, rule, lr, eps, accum)
+    if workspace is None:
+        workspace = torch.empty(max(dlrm_embbag_bwd_workspace_size(tb, indices, offsets, mode), 16),
+                                dtype=torch.uint8, device=grad_pooled.device)
+    _check_cuda(workspace, "workspace")
+    bags = _bags(indices, offsets, B)
+    dev = _device(*tb.tensors, *(accum or []), indices, offsets, grad_pooled, workspace, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_embbag_bwd_update(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode], grad_pooled.data_ptr(),
+                                        ctypes.byref(upd), workspace.data_ptr(), workspace.numel(),
+                                        status.data_ptr() if status is not None else None, _stream_ptr(stream, dev),
+                                        side_stream.cuda_stream if side_stream is not None else None)
+    _raise(st, "dlrm_embbag_bwd_update")
+
+
+def dlrm_hash_indices(num_rows, raw_ids, offsets, rows=None, index_dtype=None, status=None, stream=None):
+    """Raw 64-bit IDs (an int64 CUDA tensor, read as unsigned) to table rows, raw mod V_t; rows has the
+    offsets' dtype unless index_dtype says otherwise."""
+    lib = load_library()
+    T = len(num_rows)
+    B = _batch(offsets, T)
+    _check_cuda(raw_ids, "raw_ids", torch.int64)
+    _check_cuda(offsets, "offsets")
+    dt = index_dtype or offsets.dtype
+    if dt not in _ITYPES or offsets.dtype not in _ITYPES:
+        raise ValueError("rows and offsets must be int32 or int64")
+    if dt != offsets.dtype:
+        raise ValueError("rows and offsets share the index type")
+    if rows is None:
+        rows = torch.empty(raw_ids.numel(), dtype=dt, device=raw_ids.device)
+    _check_cuda(rows, "rows", dt)
+    nr = (ctypes.c_int64 * T)(*[int(v) for v in num_rows])
+    dev = _device(raw_ids, offsets, rows, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_hash_indices(nr, T, B, raw_ids.numel(), raw_ids.data_ptr() if raw_ids.numel() else None,
+                                   offsets.data_ptr(), _ITYPES[dt], rows.data_ptr() if rows.numel() else None,
+                                   status.data_ptr() if status is not None else None, _stream_ptr(stream, dev))
+    _raise(st, "dlrm_hash_indices")
+    return rows

@@ -165,8 +165,100 @@ dlrm_status dlrm_sparse_bwd_workspace_size(const dlrm_tables* tables, const dlrm
     if (st != DLRM_OK) return st;
     if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
     if (bytes == nullptr) return DLRM_ERR_INVALID_ARG;
-    *bytes = dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz);
+    *bytes = dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz, dlrm::kFromInteraction,
+                                       true);
     return DLRM_OK;
+}
+
+dlrm_status dlrm_embbag_bwd_workspace_size(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                           size_t* bytes)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (bytes == nullptr || !mode_ok(mode)) return DLRM_ERR_INVALID_ARG;
+    *bytes = dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz, dlrm::kFromPooledGrad,
+                                       mode == DLRM_POOL_MEAN);
+    return DLRM_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the row-update entry points; fills everything of the
+// parameter block but the interaction inputs.
+dlrm_status pack_update(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                        const dlrm_update* upd, void* workspace, int32_t* status_dev)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (tables->dtype != DLRM_F32) return DLRM_ERR_UNSUPPORTED;
+    if (!mode_ok(mode) || upd == nullptr || workspace == nullptr || !aligned16(workspace)) return DLRM_ERR_INVALID_ARG;
+    if (upd->rule != DLRM_RULE_ADAGRAD && upd->rule != DLRM_RULE_SGD) return DLRM_ERR_INVALID_ARG;
+    if (upd->rule == DLRM_RULE_ADAGRAD && upd->accum == nullptr) return DLRM_ERR_INVALID_ARG;
+    int64_t total_rows = 0;
+    for (int i = 0; i < tables->num_tables; ++i) total_rows += tables->num_rows[i];
+    // 32-bit sort keys (global row ids, the sentinel 2^32 - 1 above them), 32-bit sort values (dP row
+    // b*T + t) and 32-bit positions in the sorted lookups
+    if (total_rows >= (int64_t{1} << 32) - 1) return DLRM_ERR_UNSUPPORTED;
+    if (int64_t{tables->num_tables} * bags->batch >= (int64_t{1} << 32)) return DLRM_ERR_UNSUPPORTED;
+    if (bags->nnz >= (int64_t{1} << 32)) return DLRM_ERR_UNSUPPORTED;
+    memset(&a, 0, sizeof a);
+    int64_t base = 0;
+    for (int i = 0; i < tables->num_tables; ++i) {
+        if (upd->rule == DLRM_RULE_ADAGRAD) {
+            if (upd->accum[i] == nullptr || !aligned16(upd->accum[i])) return DLRM_ERR_INVALID_ARG;
+            a.accum[i] = upd->accum[i];
+        }
+        a.tables[i] = static_cast<float*>(tables->data[i]);
+        a.num_rows[i] = tables->num_rows[i];
+        a.row_base[i] = base;
+        base += tables->num_rows[i];
+    }
+    a.row_base[tables->num_tables] = base;
+    a.indices = bags->indices;
+    a.offsets = bags->offsets;
+    a.status = status_dev;
+    a.B = bags->batch;
+    a.nnz = bags->nnz;
+    a.T = tables->num_tables;
+    a.mean = mode == DLRM_POOL_MEAN;
+    a.lr = upd->lr;
+    a.eps = upd->eps;
+    a.rule = upd->rule;
+    a.t_magic = a.T >= 2 ? ~uint64_t{0} / static_cast<uint64_t>(a.T) + 1 : 0;
+    return DLRM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dlrm_status dlrm_sparse_bwd_update(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                   const float* dense, const float* pooled_saved, const float* grad_out,
+                                   float* grad_dense, const dlrm_update* update, void* workspace,
+                                   size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
+                                   cudaStream_t side_stream)
+{
+    BwdArgs a;
+    dlrm_status st = pack_update(a, tables, bags, mode, update, workspace, status_dev);
+    if (st != DLRM_OK) return st;
+    if (dense == nullptr || pooled_saved == nullptr || grad_out == nullptr || grad_dense == nullptr)
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned16(dense) || !aligned16(pooled_saved) || !aligned16(grad_dense) ||
+        (reinterpret_cast<uintptr_t>(grad_out) & 3u))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz,
+                                                    dlrm::kFromInteraction, true))
+        return DLRM_ERR_INVALID_ARG;
+    a.dense = dense;
+    a.pooled = pooled_saved;
+    a.grad_out = grad_out;
+    a.grad_dense = grad_dense;
+    return dlrm::launch_backward(a, tables->dim, bags->index_type, dlrm::kFromInteraction, nullptr, workspace,
+                                 workspace_bytes, stream, side_stream);
 }
 
 dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
@@ -175,56 +267,133 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* 
                                     size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
                                     cudaStream_t side_stream)
 {
-    dlrm_status st = check_tables(tables);
+    if (accum == nullptr) return DLRM_ERR_INVALID_ARG;
+    const dlrm_update upd = {DLRM_RULE_ADAGRAD, lr, eps, accum};
+    return dlrm_sparse_bwd_update(tables, bags, mode, dense, pooled_saved, grad_out, grad_dense, &upd, workspace,
+                                  workspace_bytes, status_dev, stream, side_stream);
+}
+
+dlrm_status dlrm_embbag_bwd_update(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                   const float* grad_pooled, const dlrm_update* update, void* workspace,
+                                   size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
+                                   cudaStream_t side_stream)
+{
+    BwdArgs a;
+    dlrm_status st = pack_update(a, tables, bags, mode, update, workspace, status_dev);
     if (st != DLRM_OK) return st;
-    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
-    if (tables->dtype != DLRM_F32) return DLRM_ERR_UNSUPPORTED;
-    if (!mode_ok(mode) || dense == nullptr || pooled_saved == nullptr || grad_out == nullptr ||
-        grad_dense == nullptr || accum == nullptr || workspace == nullptr)
+    if (grad_pooled == nullptr || !aligned16(grad_pooled)) return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz,
+                                                    dlrm::kFromPooledGrad, mode == DLRM_POOL_MEAN))
         return DLRM_ERR_INVALID_ARG;
-    if (!aligned16(dense) || !aligned16(pooled_saved) || !aligned16(grad_dense) || !aligned16(workspace) ||
+    return dlrm::launch_backward(a, tables->dim, bags->index_type, dlrm::kFromPooledGrad, grad_pooled, workspace,
+                                 workspace_bytes, stream, side_stream);
+}
+
+dlrm_status dlrm_interact_bwd(const float* dense, const float* pooled, const float* grad_out, int64_t batch,
+                              int32_t num_tables, int32_t dim, float* grad_dense, float* grad_pooled,
+                              cudaStream_t stream)
+{
+    if (dense == nullptr || pooled == nullptr || grad_out == nullptr || grad_dense == nullptr ||
+        grad_pooled == nullptr)
+        return DLRM_ERR_INVALID_ARG;
+    if (!aligned16(dense) || !aligned16(pooled) || !aligned16(grad_dense) || !aligned16(grad_pooled) ||
         (reinterpret_cast<uintptr_t>(grad_out) & 3u))
         return DLRM_ERR_INVALID_ARG;
-    const int64_t total_rows = [&] {
-        int64_t s = 0;
-        for (int i = 0; i < tables->num_tables; ++i) s += tables->num_rows[i];
-        return s;
-    }();
-    // 32-bit sort keys (global row ids, the sentinel 2^32 - 1 above them), 32-bit sort values (dP row
-    // b*T + t) and 32-bit positions in the sorted lookups
-    if (total_rows >= (int64_t{1} << 32) - 1) return DLRM_ERR_UNSUPPORTED;
-    if (int64_t{tables->num_tables} * bags->batch >= (int64_t{1} << 32)) return DLRM_ERR_UNSUPPORTED;
-    if (bags->nnz >= (int64_t{1} << 32)) return DLRM_ERR_UNSUPPORTED;
-    if (workspace_bytes < dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz))
+    if (batch < 1 || batch > (int64_t{1} << 40) || num_tables < 1 || num_tables > DLRM_MAX_TABLES)
         return DLRM_ERR_INVALID_ARG;
+    if (dim <= 0 || dim > 256 || dim % 4 != 0) return DLRM_ERR_INVALID_ARG;
+    if (!dim_supported(dim)) return DLRM_ERR_UNSUPPORTED;
     BwdArgs a;
     memset(&a, 0, sizeof a);
-    int64_t base = 0;
-    for (int i = 0; i < tables->num_tables; ++i) {
-        if (accum[i] == nullptr || !aligned16(accum[i])) return DLRM_ERR_INVALID_ARG;
-        a.tables[i] = static_cast<float*>(tables->data[i]);
-        a.accum[i] = accum[i];
-        a.num_rows[i] = tables->num_rows[i];
-        a.row_base[i] = base;
-        base += tables->num_rows[i];
-    }
-    a.row_base[tables->num_tables] = base;
-    a.indices = bags->indices;
-    a.offsets = bags->offsets;
     a.dense = dense;
-    a.pooled = pooled_saved;
+    a.pooled = pooled;
     a.grad_out = grad_out;
     a.grad_dense = grad_dense;
+    a.B = batch;
+    a.T = num_tables;
+    return dlrm::launch_interact_backward(a, dim, grad_pooled, stream);
+}
+
+dlrm_status dlrm_pooled_exchange(const dlrm_shard_plan* plan, float* const* by_table, float* const* by_sample,
+                                 int32_t to_sample, cudaStream_t stream)
+{
+    if (plan == nullptr || by_table == nullptr || by_sample == nullptr) return DLRM_ERR_INVALID_ARG;
+    const int G = plan->num_table_shards, H = plan->num_sample_shards, T = plan->num_tables, D = plan->dim;
+    if (G < 1 || G > DLRM_MAX_SHARDS || H < 1 || H > DLRM_MAX_SHARDS || T < 1 || T > DLRM_MAX_TABLES)
+        return DLRM_ERR_INVALID_ARG;
+    if (plan->batch < 1 || plan->batch > (int64_t{1} << 40) / T) return DLRM_ERR_INVALID_ARG;
+    if (plan->table_shard == nullptr || plan->table_slot == nullptr || plan->sample_start == nullptr)
+        return DLRM_ERR_INVALID_ARG;
+    if (D <= 0 || D > 256 || D % 4 != 0) return DLRM_ERR_INVALID_ARG;
+    if (!dim_supported(D)) return DLRM_ERR_UNSUPPORTED;
+    if (to_sample != 0 && to_sample != 1) return DLRM_ERR_INVALID_ARG;
+    dlrm::ExchangeArgs a;
+    memset(&a, 0, sizeof a);
+    // every shard's slots are 0 .. T_g - 1, each once
+    bool seen[DLRM_MAX_TABLES] = {};
+    for (int t = 0; t < T; ++t) {
+        const int g = plan->table_shard[t];
+        if (g < 0 || g >= G) return DLRM_ERR_INVALID_ARG;
+        a.table_shard[t] = g;
+        a.shard_tables[g] += 1;
+    }
+    for (int g = 0; g < G; ++g) {
+        for (int k = 0; k < T; ++k) seen[k] = false;
+        for (int t = 0; t < T; ++t) {
+            if (plan->table_shard[t] != g) continue;
+            const int slot = plan->table_slot[t];
+            if (slot < 0 || slot >= a.shard_tables[g] || seen[slot]) return DLRM_ERR_INVALID_ARG;
+            seen[slot] = true;
+            a.table_slot[t] = slot;
+        }
+        if (a.shard_tables[g] > 0 && (by_table[g] == nullptr || !aligned16(by_table[g]))) return DLRM_ERR_INVALID_ARG;
+        a.by_table[g] = by_table[g];
+    }
+    if (plan->sample_start[0] != 0 || plan->sample_start[H] != plan->batch) return DLRM_ERR_INVALID_ARG;
+    for (int h = 0; h < H; ++h) {
+        const int64_t n = plan->sample_start[h + 1] - plan->sample_start[h];
+        if (n < 0) return DLRM_ERR_INVALID_ARG;
+        if (n > 0 && (by_sample[h] == nullptr || !aligned16(by_sample[h]))) return DLRM_ERR_INVALID_ARG;
+        a.by_sample[h] = by_sample[h];
+        a.sample_start[h] = plan->sample_start[h];
+    }
+    a.sample_start[H] = plan->batch;
+    a.batch = plan->batch;
+    a.T = T;
+    a.G = G;
+    a.H = H;
+    a.D = D;
+    a.to_sample = to_sample;
+    return dlrm::launch_exchange(a, stream);
+}
+
+dlrm_status dlrm_hash_indices(const int64_t* num_rows, int32_t num_tables, int64_t batch, int64_t nnz,
+                              const uint64_t* raw_ids, const void* offsets, int32_t index_type, void* rows,
+                              int32_t* status_dev, cudaStream_t stream)
+{
+    if (num_rows == nullptr || offsets == nullptr || num_tables < 1 || num_tables > DLRM_MAX_TABLES)
+        return DLRM_ERR_INVALID_ARG;
+    if (batch < 1 || nnz < 0 || batch > (int64_t{1} << 40) / num_tables) return DLRM_ERR_INVALID_ARG;
+    if (nnz > 0 && (raw_ids == nullptr || rows == nullptr)) return DLRM_ERR_INVALID_ARG;
+    if (index_type != DLRM_I32 && index_type != DLRM_I64) return DLRM_ERR_INVALID_ARG;
+    if (index_type == DLRM_I32 && (nnz > INT32_MAX || int64_t{num_tables} * batch + 1 > INT32_MAX))
+        return DLRM_ERR_INVALID_ARG;
+    dlrm::HashArgs a;
+    memset(&a, 0, sizeof a);
+    for (int t = 0; t < num_tables; ++t) {
+        if (num_rows[t] < 1) return DLRM_ERR_INVALID_ARG;
+        if (index_type == DLRM_I32 && num_rows[t] > int64_t{INT32_MAX} + 1) return DLRM_ERR_INVALID_ARG;
+        a.num_rows[t] = static_cast<uint64_t>(num_rows[t]);
+        a.magic[t] = ~uint64_t{0} / a.num_rows[t];
+    }
+    a.raw = raw_ids;
+    a.offsets = offsets;
+    a.rows = rows;
     a.status = status_dev;
-    a.B = bags->batch;
-    a.nnz = bags->nnz;
-    a.T = tables->num_tables;
-    a.mean = mode == DLRM_POOL_MEAN;
-    a.lr = lr;
-    a.eps = eps;
-    a.t_magic = a.T >= 2 ? ~uint64_t{0} / static_cast<uint64_t>(a.T) + 1 : 0;
-    return dlrm::launch_backward(a, tables->dim, bags->index_type, workspace, workspace_bytes, stream,
-                                 side_stream);
+    a.B = batch;
+    a.nnz = nnz;
+    a.T = num_tables;
+    return dlrm::launch_hash(a, index_type, stream);
 }
 
 }  // extern "C"

@@ -42,7 +42,8 @@ struct Workspace {
     int64_t num_tiles, num_chunks;
 };
 
-Workspace carve(void* base, int64_t B, int32_t T, int32_t D, int64_t nnz, size_t* total)
+// with_dP: the workspace holds dP (the training step, or a scaled copy of a given pooled gradient).
+Workspace carve(void* base, int64_t B, int32_t T, int32_t D, int64_t nnz, bool with_dP, size_t* total)
 {
     Workspace w{};
     w.num_tiles = (nnz + kSortTile - 1) / kSortTile;
@@ -53,7 +54,7 @@ Workspace carve(void* base, int64_t B, int32_t T, int32_t D, int64_t nnz, size_t
         o = align256(o + bytes);
         return at;
     };
-    const size_t o_dP = take(sizeof(float) * B * T * D);
+    const size_t o_dP = with_dP ? take(sizeof(float) * B * T * D) : 0;
     size_t o_k[2], o_v[2];
     for (int i = 0; i < 2; ++i) {
         o_k[i] = take(sizeof(uint32_t) * nnz);
@@ -65,7 +66,7 @@ Workspace carve(void* base, int64_t B, int32_t T, int32_t D, int64_t nnz, size_t
     if (total) *total = o;
     if (base) {
         char* p = static_cast<char*>(base);
-        w.dP = reinterpret_cast<float*>(p + o_dP);
+        w.dP = with_dP ? reinterpret_cast<float*>(p + o_dP) : nullptr;
         for (int i = 0; i < 2; ++i) {
             w.keys[i] = reinterpret_cast<uint32_t*>(p + o_k[i]);
             w.vals[i] = reinterpret_cast<uint32_t*>(p + o_v[i]);
@@ -244,6 +245,29 @@ __global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) inte
                 }
             }
         }
+    }
+}
+
+// A given pooled gradient in mean mode: dP[b][t] = grad_pooled[b][t] / L(t,b),
+// each element one correctly rounded division, as the interaction backward
+// does it; the per-row sums then stay plain sums.  One thread per 16 bytes.
+template <typename TI>
+__global__ void __launch_bounds__(256) scale_by_bag_length_kernel(const __grid_constant__ BwdArgs a,
+                                                                  const float* __restrict__ src,
+                                                                  float* __restrict__ dst, int D)
+{
+    const int64_t n4 = a.B * a.T * (D / 4);
+    for (int64_t e = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; e < n4; e += int64_t{gridDim.x} * blockDim.x) {
+        const int64_t row = e / (D / 4);  // b * T + t
+        const int64_t b = row / a.T, t = row - b * a.T;
+        const int64_t bag = t * a.B + b;
+        const int64_t L = ld_index<TI>(a.offsets, bag + 1) - ld_index<TI>(a.offsets, bag);
+        float4 v = reinterpret_cast<const float4*>(src)[e];
+        if (L > 0) {
+            const float fl = static_cast<float>(L);
+            v = make_float4(__fdiv_rn(v.x, fl), __fdiv_rn(v.y, fl), __fdiv_rn(v.z, fl), __fdiv_rn(v.w, fl));
+        }
+        reinterpret_cast<float4*>(dst)[e] = v;
     }
 }
 
@@ -550,12 +574,25 @@ __device__ __forceinline__ void add4(float4& g, float4 v)
     g = make_float4(a.x, a.y, b.x, b.y);
 }
 
+// One update of the row `key` of table t whose summed gradient (this lane's slice) is g:
+//   Adagrad (row-wise): A += mean_d g_d^2, w -= lr g / (sqrt(A) + eps);   SGD: w -= lr g.
 template <int D>
 __device__ __forceinline__ void adagrad_row(const BwdArgs& a, uint32_t key, int t, const float4 (&g)[Lanes<D>::kChunks],
                                             int lane)
 {
     constexpr int C = Lanes<D>::kChunks;
     const bool active = lane < Lanes<D>::kActive;
+    if (a.rule == DLRM_RULE_SGD) {
+        if (active) {
+            float* w = a.tables[t] + (static_cast<int64_t>(key) - a.row_base[t]) * D;
+#pragma unroll
+            for (int k = 0; k < C; ++k) {
+                const int col = (lane + k * kWarp) * 4;
+                *reinterpret_cast<float4*>(w + col) = step_row(*reinterpret_cast<const float4*>(w + col), g[k], a.lr);
+            }
+        }
+        return;
+    }
     float ss = 0.0f;
     if (active) {
 #pragma unroll
@@ -588,9 +625,9 @@ __device__ __forceinline__ uint32_t div_by_T(uint32_t v, const BwdArgs& a)
     return a.T == 1 ? v : static_cast<uint32_t>(__umul64hi(static_cast<uint64_t>(v), a.t_magic));
 }
 
-// Row-wise Adagrad on one row whose weights (this lane's slice) and
-// accumulator were read earlier: w is the row before the step, acc_old its
-// accumulator.
+// The update of one row whose weights (this lane's slice) and accumulator
+// were read earlier: w is the row before the step, acc_old its accumulator
+// (Adagrad only).
 template <int D>
 __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, int t,
                                               const float4 (&g)[Lanes<D>::kChunks],
@@ -598,6 +635,15 @@ __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, in
 {
     constexpr int C = Lanes<D>::kChunks;
     const bool active = lane < Lanes<D>::kActive;
+    if (a.rule == DLRM_RULE_SGD) {
+        if (active) {
+            float* wr = a.tables[t] + (static_cast<int64_t>(key) - a.row_base[t]) * D;
+#pragma unroll
+            for (int k = 0; k < C; ++k)
+                *reinterpret_cast<float4*>(wr + (lane + k * kWarp) * 4) = step_row(w[k], g[k], a.lr);
+        }
+        return;
+    }
     float ss = 0.0f;
     if (active) {
 #pragma unroll
@@ -694,7 +740,7 @@ __global__ void __launch_bounds__(kSegThreads, D >= 256 ? 4 : 8) segment_chunk_k
                         const uint32_t b = div_by_T(vj, a);
                         tj[u] = static_cast<int>(vj - b * static_cast<uint32_t>(a.T));
                         const int64_t r = static_cast<int64_t>(kj[u]) - a.row_base[tj[u]];
-                        ap[u] = a.accum[tj[u]][r];
+                        ap[u] = a.rule == DLRM_RULE_ADAGRAD ? a.accum[tj[u]][r] : 0.0f;
                         if (active) {
                             const float* wr = a.tables[tj[u]] + r * D;
 #pragma unroll
@@ -872,7 +918,20 @@ struct Fork {
 };
 
 template <int D, typename TI>
-dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s, cudaStream_t side)
+dlrm_status launch_interact_bwd_groups(const BwdArgs& a, float* dP, cudaStream_t s)
+{
+    // warps per sample: one per 8-row block of dV up to 4 (N <= 32), else 8; a sample's V is staged once
+    const int nblk = round_up(a.T + 1, 8) / 8;
+    return nblk > 4   ? launch_interact_bwd<D, 8, TI>(a, dP, s)
+           : nblk > 2 ? launch_interact_bwd<D, 4, TI>(a, dP, s)
+                      : launch_interact_bwd<D, 1, TI>(a, dP, s);
+}
+
+// The training step (source kFromInteraction: dP from the interaction backward, already divided by the
+// bag lengths in mean mode) or the row update from a given pooled gradient (kFromPooledGrad).
+template <int D, typename TI>
+dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const float* grad_pooled, cudaStream_t s,
+                         cudaStream_t side)
 {
     Fork f;
     const bool two = side != nullptr && side != s && a.nnz > 0;
@@ -884,13 +943,19 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s, c
 
     int cur = 0;
     dlrm_status st = a.nnz > 0 ? sort_keys<TI>(a, w, ks, &cur) : DLRM_OK;
-    // interaction backward (warps per sample: one per 8-row block of dV up to 4 (N <= 32), else 8; a
-    // sample's V is staged once)
+    // beside the sort: the dP rows the per-row sums read
+    const float* dP = source == kFromInteraction ? w.dP : grad_pooled;
     if (st == DLRM_OK) {
-        const int nblk = round_up(a.T + 1, 8) / 8;
-        st = nblk > 4   ? launch_interact_bwd<D, 8, TI>(a, w.dP, s)
-             : nblk > 2 ? launch_interact_bwd<D, 4, TI>(a, w.dP, s)
-                        : launch_interact_bwd<D, 1, TI>(a, w.dP, s);
+        if (source == kFromInteraction) {
+            st = launch_interact_bwd_groups<D, TI>(a, w.dP, s);
+        } else if (a.mean && a.nnz > 0) {
+            const int64_t n4 = a.B * a.T * (D / 4);
+            const int64_t blocks = (n4 + 255) / 256;
+            scale_by_bag_length_kernel<TI><<<static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, s>>>(
+                a, grad_pooled, w.dP, D);
+            dP = w.dP;
+            st = cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
+        }
     }
     // the side stream's work joins the caller's stream whatever happened above
     if (two && (cudaEventRecord(f.join, side) != cudaSuccess || cudaStreamWaitEvent(s, f.join, 0) != cudaSuccess))
@@ -898,39 +963,56 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, cudaStream_t s, c
     if (st != DLRM_OK || a.nnz == 0) return st;
 
     const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + kSegThreads / kWarp - 1) / (kSegThreads / kWarp));
-    segment_chunk_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], w.dP, w.partial,
+    segment_chunk_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], dP, w.partial,
                                                                w.num_chunks);
     segment_span_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], w.partial, w.num_chunks);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
 template <int D>
-dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, cudaStream_t s, cudaStream_t side)
+dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, int source, const float* grad_pooled,
+                         cudaStream_t s, cudaStream_t side)
 {
-    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, s, side) : run_backward<D, int64_t>(a, w, s, side);
+    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, source, grad_pooled, s, side)
+                                  : run_backward<D, int64_t>(a, w, source, grad_pooled, s, side);
 }
+
+bool with_dP(int source, bool mean) { return source == kFromInteraction || mean; }
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz)
+size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz, int source, bool mean)
 {
     size_t total = 0;
-    carve(nullptr, B, T, D, nnz, &total);
+    carve(nullptr, B, T, D, nnz, with_dP(source, mean), &total);
     return total;
 }
 
-dlrm_status launch_backward(const BwdArgs& a, int dim, int index_type, void* workspace, size_t workspace_bytes,
-                            cudaStream_t s, cudaStream_t side)
+dlrm_status launch_backward(const BwdArgs& a, int dim, int index_type, int source, const float* grad_pooled,
+                            void* workspace, size_t workspace_bytes, cudaStream_t s, cudaStream_t side)
 {
     size_t need = 0;
-    const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, &need);
+    const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, with_dP(source, a.mean != 0), &need);
     if (workspace_bytes < need) return DLRM_ERR_INVALID_ARG;
     switch (dim) {
-        case 16: return dispatch_bwd<16>(a, index_type, w, s, side);
-        case 32: return dispatch_bwd<32>(a, index_type, w, s, side);
-        case 64: return dispatch_bwd<64>(a, index_type, w, s, side);
-        case 128: return dispatch_bwd<128>(a, index_type, w, s, side);
-        case 256: return dispatch_bwd<256>(a, index_type, w, s, side);
+        case 16: return dispatch_bwd<16>(a, index_type, w, source, grad_pooled, s, side);
+        case 32: return dispatch_bwd<32>(a, index_type, w, source, grad_pooled, s, side);
+        case 64: return dispatch_bwd<64>(a, index_type, w, source, grad_pooled, s, side);
+        case 128: return dispatch_bwd<128>(a, index_type, w, source, grad_pooled, s, side);
+        case 256: return dispatch_bwd<256>(a, index_type, w, source, grad_pooled, s, side);
+        default: return DLRM_ERR_UNSUPPORTED;
+    }
+}
+
+dlrm_status launch_interact_backward(const BwdArgs& a, int dim, float* grad_pooled, cudaStream_t s)
+{
+    // no bag lengths are applied (a.mean is 0), so the offsets are never read
+    switch (dim) {
+        case 16: return launch_interact_bwd_groups<16, int32_t>(a, grad_pooled, s);
+        case 32: return launch_interact_bwd_groups<32, int32_t>(a, grad_pooled, s);
+        case 64: return launch_interact_bwd_groups<64, int32_t>(a, grad_pooled, s);
+        case 128: return launch_interact_bwd_groups<128, int32_t>(a, grad_pooled, s);
+        case 256: return launch_interact_bwd_groups<256, int32_t>(a, grad_pooled, s);
         default: return DLRM_ERR_UNSUPPORTED;
     }
 }

@@ -69,13 +69,55 @@ struct BwdArgs {
     int32_t mean;
     float lr;
     float eps;
+    int32_t rule;      // DLRM_RULE_ADAGRAD or DLRM_RULE_SGD
     uint64_t t_magic;  // ceil(2^64 / T) for T >= 2: sort value v = b*T + t gives b = high word of v * t_magic
 };
 
-size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz);
+// Where the gradient of the pooled vectors comes from.
+enum BwdSource : int {
+    kFromInteraction = 0,  // the interaction backward of this call (dense, pooled, grad_out)
+    kFromPooledGrad = 1,   // the caller's grad_pooled [B][T][D]
+};
+
+// Workspace bytes of the training step (source kFromInteraction) or of the row
+// update from a given pooled gradient (kFromPooledGrad, mean pooling needs a
+// scaled copy of it).
+size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz, int source, bool mean);
 
 // side: a second stream for the key build and sort (nullptr or == stream: one stream).
-dlrm_status launch_backward(const BwdArgs& args, int dim, int index_type, void* workspace,
-                            size_t workspace_bytes, cudaStream_t stream, cudaStream_t side);
+// grad_pooled: the source of kFromPooledGrad (ignored otherwise).
+dlrm_status launch_backward(const BwdArgs& args, int dim, int index_type, int source, const float* grad_pooled,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream, cudaStream_t side);
+
+// The interaction backward alone: grad_dense and grad_pooled (not scaled by bag lengths).
+dlrm_status launch_interact_backward(const BwdArgs& args, int dim, float* grad_pooled, cudaStream_t stream);
+
+// Raw IDs to rows: rows[p] = raw[p] mod V_t (unsigned), t the table holding position p.
+struct HashArgs {
+    uint64_t num_rows[DLRM_MAX_TABLES];
+    uint64_t magic[DLRM_MAX_TABLES];  // floor((2^64 - 1) / V_t)
+    const uint64_t* raw;
+    const void* offsets;
+    void* rows;
+    int32_t* status;
+    int64_t B;
+    int64_t nnz;
+    int32_t T;
+};
+dlrm_status launch_hash(const HashArgs& args, int index_type, cudaStream_t stream);
+
+// The exchange of pooled vectors between G table shards and H sample shards.
+struct ExchangeArgs {
+    float* by_table[DLRM_MAX_SHARDS];   // table shard g: batch x shard_tables[g] x D
+    float* by_sample[DLRM_MAX_SHARDS];  // sample shard h: (sample_start[h+1] - sample_start[h]) x T x D
+    int64_t sample_start[DLRM_MAX_SHARDS + 1];
+    int32_t table_shard[DLRM_MAX_TABLES];
+    int32_t table_slot[DLRM_MAX_TABLES];
+    int32_t shard_tables[DLRM_MAX_SHARDS];
+    int64_t batch;
+    int32_t T, G, H, D;
+    int32_t to_sample;  // 1: by_table -> by_sample, 0: by_sample -> by_table
+};
+dlrm_status launch_exchange(const ExchangeArgs& args, cudaStream_t stream);
 
 }  // namespace dlrm

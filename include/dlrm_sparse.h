@@ -140,6 +140,24 @@ dlrm_status dlrm_sparse_fwd_host(const dlrm_tables *tables, const dlrm_bags *bag
                                  float *out_dev, int32_t *status_dev,
                                  cudaStream_t stream);
 
+/* Update rules of the embedding rows ("DLRM", robocikowo.com, "Forward
+ * pass", last sentence: training with SGD or Adagrad).  Both act on g_r, the
+ * sum over the step's lookups of row r of the gradient of the pooled vector
+ * of the lookup's bag (times 1/L in mean mode), once per touched row:
+ *   DLRM_RULE_ADAGRAD  row-wise Adagrad: A_r += mean_d(g_r,d^2);
+ *                      w_r,d -= lr * g_r,d / (sqrt(A_r) + eps)
+ *   DLRM_RULE_SGD      plain SGD: w_r,d -= lr * g_r,d (no momentum, no decay)
+ * Rows that no lookup of the batch touches are left unchanged. */
+typedef enum { DLRM_RULE_ADAGRAD = 0, DLRM_RULE_SGD = 1 } dlrm_update_rule;
+
+typedef struct {
+    int32_t rule;               /* dlrm_update_rule */
+    float lr;                   /* learning rate */
+    float eps;                  /* Adagrad: added to sqrt(A_r) */
+    float *const *accum;        /* Adagrad: HOST array of T device pointers, V_t fp32
+                                 * accumulators each, updated in place; SGD: unused */
+} dlrm_update;
+
 /* Bytes of device workspace dlrm_sparse_bwd_adagrad needs for these shapes. */
 dlrm_status dlrm_sparse_bwd_workspace_size(const dlrm_tables *tables,
                                            const dlrm_bags *bags,
@@ -180,6 +198,112 @@ dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables *tables, const dlrm_bags *
                                     void *workspace, size_t workspace_bytes,
                                     int32_t *status_dev, cudaStream_t stream,
                                     cudaStream_t side_stream);
+
+/* The training step of dlrm_sparse_bwd_adagrad with either update rule
+ * (update->rule; update->accum only for Adagrad).  Arguments, workspace
+ * (dlrm_sparse_bwd_workspace_size), streams, limits and errors as there;
+ * DLRM_ERR_INVALID_ARG for an unknown rule or Adagrad without accumulators. */
+dlrm_status dlrm_sparse_bwd_update(const dlrm_tables *tables, const dlrm_bags *bags,
+                                   dlrm_pool_mode mode, const float *dense,
+                                   const float *pooled_saved, const float *grad_out,
+                                   float *grad_dense, const dlrm_update *update,
+                                   void *workspace, size_t workspace_bytes,
+                                   int32_t *status_dev, cudaStream_t stream,
+                                   cudaStream_t side_stream);
+
+/* The interaction backward alone (calculus on "DLRM", robocikowo.com,
+ * "Forward pass" steps (3)-(4)): with g(i,j) = g(j,i) = grad_out[b][D + pos(i,j)],
+ *   dV_i = sum_{j != i} g(i,j) V_j,  grad_dense = grad_out[b][0:D] + dV_0,
+ *   grad_pooled[b][t] = dV_{1+t}   (the gradient of the pooled vector itself:
+ *                                   no bag length is applied here).
+ * dense: device B x D; pooled: device B x T x D; grad_out: device
+ * B x (D + N(N-1)/2); grad_dense: device B x D and grad_pooled: device
+ * B x T x D, written.  fp32 throughout; batch = B >= 1, num_tables = T in
+ * [1, DLRM_MAX_TABLES], dim = D as for the tables.  Together with
+ * dlrm_embbag_bwd_update it is the training step split at the pooled vectors,
+ * the point where a model-parallel step exchanges them between devices. */
+dlrm_status dlrm_interact_bwd(const float *dense, const float *pooled, const float *grad_out,
+                              int64_t batch, int32_t num_tables, int32_t dim,
+                              float *grad_dense, float *grad_pooled, cudaStream_t stream);
+
+/* Bytes of device workspace dlrm_embbag_bwd_update needs for these shapes
+ * (mean pooling needs a scaled copy of grad_pooled). */
+dlrm_status dlrm_embbag_bwd_workspace_size(const dlrm_tables *tables, const dlrm_bags *bags,
+                                           dlrm_pool_mode mode, size_t *bytes);
+
+/* Steps 2-3 of the training step from a given gradient of the pooled
+ * vectors: per touched row r, g_r = sum of grad_pooled[b][t] (times 1/L in
+ * mean mode) over the lookups of r, reduced in lookup order after a stable
+ * radix sort by row (bitwise reproducible run to run), then one update of
+ * the row by update->rule, in place.  tables (fp32, updated in place) and bags
+ * as for the forward; grad_pooled: device B x T x D fp32, 16-byte aligned.
+ * workspace: device, >= dlrm_embbag_bwd_workspace_size() bytes.  Streams,
+ * limits and errors as for dlrm_sparse_bwd_adagrad. */
+dlrm_status dlrm_embbag_bwd_update(const dlrm_tables *tables, const dlrm_bags *bags,
+                                   dlrm_pool_mode mode, const float *grad_pooled,
+                                   const dlrm_update *update, void *workspace,
+                                   size_t workspace_bytes, int32_t *status_dev,
+                                   cudaStream_t stream, cudaStream_t side_stream);
+
+/* The raw-ID hashing pre-pass ("Deep Learning Recommendation Model (DLRM)",
+ * notes.helloworld.co.in, "Why it is mostly a systems problem": IDs hashed
+ * into tables of a fixed number of rows), in its plainest form, a modulo:
+ *   rows[p] = raw_ids[p] mod V_t   (raw_ids read as unsigned 64-bit),
+ * t the table whose bags hold position p: the last t with
+ * offsets[t*B] <= p.  num_rows: HOST array of T values V_t >= 1 (at most
+ * 2^31 for DLRM_I32 output).  raw_ids: device, nnz entries; offsets: device,
+ * T*B+1 table-major CSR offsets of index_type; rows: device, nnz entries of
+ * index_type, written (ready to serve as the bags' indices).  A position in
+ * no table's range, or table boundaries that go backwards, set
+ * DLRM_ERR_BAD_OFFSETS in *status_dev (such a position gets row 0). */
+dlrm_status dlrm_hash_indices(const int64_t *num_rows, int32_t num_tables, int64_t batch,
+                              int64_t nnz, const uint64_t *raw_ids, const void *offsets,
+                              int32_t index_type, void *rows, int32_t *status_dev,
+                              cudaStream_t stream);
+
+/* ---- table-wise model parallelism ---------------------------------------
+ * "DLRM" (robocikowo.com), hybrid-parallelism paragraph: the embedding tables
+ * are split across devices (model parallel) while the MLPs run data
+ * parallel, and the lookup results pass through an all-to-all before the
+ * interaction layer; "DLRM explained", "How do you size compute for a
+ * DLRM...": tables sharded across devices, an NCCL all-to-all between them.
+ *
+ * A plan splits the T tables among G table shards (shard g owns T_g tables,
+ * pools them for all B samples into a B x T_g x D buffer, in the order of
+ * its tables' slots) and the B samples among H sample shards (shard h owns
+ * samples [sample_start[h], sample_start[h+1]) and runs the interaction on a
+ * (sample_start[h+1] - sample_start[h]) x T x D buffer, tables in global
+ * order).  All arrays are HOST memory. */
+#define DLRM_MAX_SHARDS 64
+
+typedef struct {
+    int32_t num_table_shards;     /* G in [1, DLRM_MAX_SHARDS] */
+    int32_t num_sample_shards;    /* H in [1, DLRM_MAX_SHARDS] */
+    int32_t num_tables;           /* T in [1, DLRM_MAX_TABLES] */
+    int32_t dim;                  /* D, as for the tables */
+    int64_t batch;                /* B >= 1: samples of the by-table buffers */
+    const int32_t *table_shard;   /* [T]: the shard g that owns table t */
+    const int32_t *table_slot;    /* [T]: t's position among the tables of its shard; the
+                                   * slots of a shard are 0 .. T_g - 1, each once */
+    const int64_t *sample_start;  /* [H + 1]: 0 = sample_start[0] <= ... <= sample_start[H] = B */
+} dlrm_shard_plan;
+
+/* The all-to-all of the pooled vectors between the shards of a plan, on one
+ * device: every (sample b, table t) row moves between by_table[g][b][slot(t)]
+ * (g the owner of t) and by_sample[h][b - sample_start[h]][t] (h the sample
+ * shard of b).  to_sample = 1 copies by_table -> by_sample (the forward:
+ * pooled vectors to the interaction); to_sample = 0 copies by_sample ->
+ * by_table (the backward: gradients of the pooled vectors back to the
+ * table owners).  by_table, by_sample: HOST arrays of G and H device
+ * pointers (fp32, 16-byte aligned; NULL allowed for an empty shard); the
+ * source side is read, the other written; the two must not overlap.  With
+ * G = H shards held by this device the call is the whole exchange; after a
+ * collective all-to-all between devices, H = 1 gives the local unpack of
+ * what one device received (and to_sample = 0 the pack before the reverse
+ * collective).  DLRM_ERR_INVALID_ARG for an inconsistent plan. */
+dlrm_status dlrm_pooled_exchange(const dlrm_shard_plan *plan, float *const *by_table,
+                                 float *const *by_sample, int32_t to_sample,
+                                 cudaStream_t stream);
 
 /* Bytes of the fixed scratch behind dlrm_sparse_bwd_adagrad_static. */
 #define DLRM_STATIC_SCRATCH_BYTES (32u << 20)
