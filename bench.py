@@ -54,6 +54,13 @@ def parse():
                    help="override the batch size (a small case of the same kernels, for profiling)")
     p.add_argument("--uniform", action="store_true",
                    help="uniform instead of Zipf indices (every lookup a likely DRAM read)")
+    p.add_argument("--rule", choices=["adagrad", "sgd"], default="adagrad",
+                   help="row update rule of the training workload")
+    p.add_argument("--shards", type=int, default=1,
+                   help="G > 1: table-wise model parallelism over G logical shards on this device (the "
+                        "embedding-bag lookup per table shard, the exchange, the interaction per sample shard)")
+    p.add_argument("--hash", action="store_true",
+                   help="the bags arrive as raw 64-bit IDs: the hashing pre-pass (ID mod V_t) runs in each step")
     return p.parse_args()
 
 
@@ -89,22 +96,44 @@ def sort_passes(w: gen.Workload) -> int:
     return (bits + 8) // 9
 
 
-def train_bytes(w: gen.Workload, batch: gen.Batch) -> dict:
-    """Bytes one training step must move (int32 indices), by phase:
-    forward: looked-up rows, x, out, pooled vectors saved, indices, offsets;
-    backward: grad_out, x and pooled read, grad_dense written, dP written
-    once and read once per lookup, lookup keys written, (key, value) read
-    and written by each radix pass, and per touched row its weights and
-    accumulator read and written."""
+def train_bytes(w: gen.Workload, batch: gen.Batch, rule: str = "adagrad") -> dict:
+    """Bytes one training step must move (int32 indices), by phase.
+    forward: looked-up rows, x, out, pooled vectors saved, indices, offsets.
+    backward, two models that differ only in the reads of dP:
+      "per_bag":    dP written once and read once (a read per bag), the model the
+                    workload description uses;
+      "per_lookup": dP read once per lookup, which is what a reduction of the
+                    lookups sorted by row reads: the rows a bag's lookups touch
+                    are scattered over the sorted order, so every lookup fetches
+                    its bag's dP row, and at B*T*D*4 bytes (436 MB for the
+                    training workload) dP does not stay in the 126 MB L2.
+    Both count grad_out, x and pooled read, grad_dense written, the lookup keys
+    written, (key, value) read and written by each radix pass, and per touched
+    row its weights read and written (and for Adagrad its accumulator)."""
     nnz = batch.nnz
     BTD = w.B * w.T * w.D * 4
     off = batch.offsets.astype(np.int64)
     touched = sum(int(np.unique(batch.indices[off[t * w.B]:off[(t + 1) * w.B]]).size) for t in range(w.T))
     fwd = (nnz * w.D * w.elem_bytes + w.B * w.D * 4 + w.B * w.out_width * 4 + BTD + nnz * 4
            + (w.T * w.B + 1) * 4)
-    bwd = (w.B * w.out_width * 4 + w.B * w.D * 4 + BTD + w.B * w.D * 4 + BTD + nnz * w.D * 4 + nnz * 8
-           + sort_passes(w) * nnz * 16 + touched * (2 * w.D * 4 + 8) + nnz * 4 + (w.T * w.B + 1) * 4)
-    return {"forward": fwd, "backward": bwd, "total": fwd + bwd, "touched_rows": touched}
+    row = 2 * w.D * 4 + (8 if rule == "adagrad" else 0)
+    common = (w.B * w.out_width * 4 + w.B * w.D * 4 + BTD + w.B * w.D * 4 + BTD + nnz * 8
+              + sort_passes(w) * nnz * 16 + touched * row + nnz * 4 + (w.T * w.B + 1) * 4)
+    per_bag = common + BTD
+    per_lookup = common + nnz * w.D * 4
+    return {"forward": fwd, "backward": per_bag, "backward_per_lookup": per_lookup, "total": fwd + per_bag,
+            "touched_rows": touched}
+
+
+def hash_bytes(w: gen.Workload, batch: gen.Batch) -> int:
+    """Bytes of the hashing pre-pass: a raw 8-byte ID read and a 4-byte row written per lookup, and the
+    T + 1 table boundaries of the offsets."""
+    return batch.nnz * 12 + (w.T + 1) * 4
+
+
+def exchange_bytes(w: gen.Workload) -> int:
+    """Bytes of one exchange of the pooled vectors: every (sample, table) row read once and written once."""
+    return 2 * w.B * w.T * w.D * 4
 
 
 def peaks():
@@ -278,47 +307,66 @@ def sub_batch(w: gen.Workload, b: gen.Batch, S: int):
 class OracleStep:
     """One step of the path on the CPU oracle (plain C, OpenMP over samples):
     the fused forward, and for training also the interaction backward, the
-    per-row gradient sums and row-wise Adagrad.  Tables are host copies of the
+    per-row gradient sums and the row update.  Tables are host copies of the
     rows the batch touches."""
 
-    def __init__(self, w: gen.Workload, b: gen.Batch):
+    def __init__(self, w: gen.Workload, b: gen.Batch, rule: str = "adagrad"):
         import oracle
         self.orc = oracle.get()
-        self.w, self.b = w, b
+        self.w, self.b, self.rule = w, b, rule
         self.tabs, self.nr, self.idx = gen.compact_tables(w, b)
         if w.train:
-            self.acc = [np.full(n, w.accum_init, np.float32) for n in self.nr]
+            self.acc = [np.full(n, w.accum_init, np.float32) for n in self.nr] if rule == "adagrad" else None
 
     def __call__(self):
         w, b = self.w, self.b
         r = self.orc.sparse_fwd(self.tabs, self.nr, self.idx, b.offsets, b.dense, w.mode, w.dtype,
                                 with_pooled=w.train)
         if w.train:
-            self.orc.sparse_bwd_adagrad(self.tabs, self.nr, self.idx, b.offsets, b.dense, r["pooled"], b.grad_out,
-                                        self.acc, w.lr, w.eps, w.mode)
+            self.orc.sparse_bwd_update(self.tabs, self.nr, self.idx, b.offsets, b.dense, r["pooled"], b.grad_out,
+                                       self.rule, w.lr, w.eps, self.acc, w.mode)
 
 
-def oracle_baseline(w: gen.Workload, batch: gen.Batch, seconds: float):
-    """Time the oracle on the workload until `seconds` have passed: whole
-    batches for the forward, a 4096-sample part of one for the training step."""
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    if w.train:
-        ws, bs = sub_batch(w, batch, 4096)
-        what = f"first {ws.B} samples of one batch"
-    else:
-        ws, bs = w, batch
-        what = f"one full batch of {w.B} samples"
-    run = OracleStep(ws, bs)
-    run()  # warm
-    n, t0 = 0, time.perf_counter()
-    while True:
-        run()
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": n * ws.B / el, "unit": "samples/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} x {what} (rows the batch touches copied to host memory), {el:.1f} s"}
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def oracle_baseline(w: gen.Workload, batch: gen.Batch, seconds: float, rule: str = "adagrad"):
+    """Time the oracle on a bounded part of the workload (the first 16,384
+    samples of a forward batch, 4,096 of a training batch) at all host cores,
+    then at one thread, each for about half of `seconds`.  The thread count
+    changes no arithmetic."""
+    S = 4096 if w.train else 16384
+    ws, bs = sub_batch(w, batch, S)
+    run = OracleStep(ws, bs, rule)
+    all_threads = run.orc.set_threads(os.cpu_count() or 1)
+
+    def timed(threads, secs):
+        got = run.orc.set_threads(threads)
+        run()  # warm
+        n, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= secs:
+                return n * ws.B / el, got, f"{n} x the first {ws.B} samples of one batch, {el:.1f} s"
+
+    v_all, c_all, what_all = timed(all_threads, seconds / 2)
+    v_one, _, what_one = timed(1, seconds / 2)
+    run.orc.set_threads(all_threads)
+    return {"value": v_all, "unit": "samples/s", "cores": c_all, "kind": "oracle",
+            "sample": what_all + " (rows the batch touches copied to host memory)",
+            "one_thread": {"value": v_one, "unit": "samples/s", "sample": what_one},
+            "cpu_model": cpu_model(), "nproc": os.cpu_count()}
 
 
 def run_reference(args, w):
@@ -329,7 +377,7 @@ def run_reference(args, w):
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     # each step: a bounded sample of one batch (its first S samples), about a second of CPU work
     S = min(w.B, 4096 if w.train else 16384)
-    runs = [OracleStep(*sub_batch(w, b, S)) for b in batches]
+    runs = [OracleStep(*sub_batch(w, b, S), args.rule) for b in batches]
     for i in range(args.warmup):
         runs[i % len(runs)]()
     t0 = time.perf_counter()
@@ -357,17 +405,65 @@ def config_of(w, args):
             "rotated_batches": N_ROTATE,
             "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write, then a {DRAIN_BYTES >> 20} MB read so "
                   "the flush's dirty lines are written back outside the timed region)",
-            "parallelism": f"replicas x{args.gpus} (no data-path collective)"}
+            "parallelism": f"replicas x{args.gpus} (no data-path collective)"
+            + (f"; tables split over {args.shards} logical shards on each device (table-wise model parallel, "
+               "all-to-all by the exchange kernel)" if args.shards > 1 else ""),
+            **({"update_rule": args.rule} if w.train else {}),
+            **({"indices": "raw 64-bit IDs, hashed to rows (ID mod V_t) inside each step"} if args.hash else {})}
 
 
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+def phase_bytes(args, w: gen.Workload, b: gen.Batch) -> dict:
+    """Algorithmic bytes of each phase of one step of this configuration (int32 indices)."""
+    BTD = w.B * w.T * w.D * 4
+    rows = b.nnz * w.D * w.elem_bytes
+    csr = b.nnz * 4 + (w.T * w.B + 1) * 4
+    out = w.B * w.out_width * 4
+    x = w.B * w.D * 4
+    ph = {}
+    if args.hash:
+        ph["hash"] = hash_bytes(w, b)
+    if args.shards > 1:
+        ph["lookup"] = rows + csr + BTD
+        ph["exchange"] = exchange_bytes(w)
+        ph["interaction"] = BTD + x + out
+        if w.train:
+            tb = train_bytes(w, b, args.rule)
+            ph["interaction_bwd"] = out + x + BTD + x + BTD
+            ph["exchange_bwd"] = exchange_bytes(w)
+            ph["update"] = tb["backward"] - ph["interaction_bwd"]
+        return ph
+    if w.train:
+        tb = train_bytes(w, b, args.rule)
+        ph["forward"] = tb["forward"]
+        ph["backward"] = tb["backward"]
+    else:
+        ph["forward"] = algorithmic_bytes(w, b)
+    return ph
+
+
+def raw_ids_for(w: gen.Workload, b: gen.Batch, seed: int) -> np.ndarray:
+    """Raw 64-bit IDs whose hash (ID mod V_t) is the batch's row: row + V_t * k, k random, so the hashed
+    step looks up exactly the rows of the plain step."""
+    rng = np.random.default_rng(seed)
+    off = b.offsets.astype(np.int64)
+    raw = np.empty(b.nnz, np.uint64)
+    for t in range(w.T):
+        lo, hi = off[t * w.B], off[(t + 1) * w.B]
+        V = w.num_rows[t]
+        k = rng.integers(0, (1 << 63) // V, size=hi - lo, dtype=np.uint64)
+        raw[lo:hi] = b.indices[lo:hi].astype(np.uint64) + k * np.uint64(V)
+    return raw.view(np.int64)
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
 
     import embedding_bag_lookup_dlrm_b300 as dl
+    from embedding_bag_lookup_dlrm_b300 import sharding
 
     rank, world, local = dist_env()
     if world > 1:
@@ -375,6 +471,8 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dl.load_library()
+    if args.hash and args.shards > 1:
+        raise SystemExit("--hash and --shards together are not a configuration of this bench")
 
     # tables: filled on the device by the seeded generator
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -397,8 +495,17 @@ def run_ours(args, w):
         flush.zero_()
         drain.sum()
 
+    if args.hash:
+        raws = [torch.from_numpy(raw_ids_for(w, b, 77 + i)).to(dev) for i, b in enumerate(batches)]
+        hashed = torch.empty(max(b.nnz for b in batches), dtype=torch.int32, device=dev)
+    if args.shards > 1:
+        plan = sharding.ShardPlan.make(w.num_rows, w.D, w.B, args.shards, w.elem_bytes)
+        shard_bags = [[(torch.from_numpy(i).to(dev), torch.from_numpy(o).to(dev))
+                       for i, o in sharding.split_bags(plan, b.indices, b.offsets)] for b in batches]
+        sharded = sharding.ShardedSparse(tabs, plan)
     if w.train:
-        accum = [torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+        accum = ([torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+                 if args.rule == "adagrad" else None)
         grads = [torch.from_numpy(b.grad_out).to(dev) for b in batches]
         pooled = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device=dev)
         grad_dense = torch.empty((w.B, w.D), dtype=torch.float32, device=dev)
@@ -407,99 +514,111 @@ def run_ours(args, w):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-
-    def step(i, s, mid=None):
-        idx, off, x = dev_batches[i % N_ROTATE]
-        if not w.train:
-            dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, stream=s)
-            return
-        dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, pooled_save=pooled, stream=s)
-        if mid is not None:
-            mid.record(s)
-        dl.dlrm_sparse_bwd_adagrad(tables, accum, idx, off, x, pooled, grads[i % N_ROTATE], w.lr, w.eps, w.mode,
-                                   grad_dense=grad_dense, workspace=workspace, stream=s, side_stream=side)
-
     s = torch.cuda.Stream(device=dev)
     # the training step's key build and sort run beside its interaction backward, on a stream of the
     # highest priority so that the short dependent sort kernels get SMs as soon as any free up
     side = torch.cuda.Stream(device=dev, priority=-100)
+
+    def step(i, rec):
+        """Queue step i on stream s; rec(name) records the end of a phase."""
+        k = i % N_ROTATE
+        idx, off, x = dev_batches[k]
+        if args.hash:
+            idx = dl.dlrm_hash_indices(w.num_rows, raws[k], off, rows=hashed[:raws[k].numel()], stream=s)
+            rec("hash")
+        if args.shards > 1:
+            sharded.forward(shard_bags[k], x, w.mode, out=out, stream=s, after=rec)
+            if w.train:
+                sharded.backward(shard_bags[k], x, grads[k], args.rule, w.lr, w.eps, accum, w.mode,
+                                 grad_dense=grad_dense, stream=s, side_stream=side, after=rec)
+            return
+        if not w.train:
+            dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, stream=s)
+            rec("forward")
+            return
+        dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, pooled_save=pooled, stream=s)
+        rec("forward")
+        dl.dlrm_sparse_bwd_update(tables, idx, off, x, pooled, grads[k], args.rule, w.lr, w.eps, accum, w.mode,
+                                  grad_dense=grad_dense, workspace=workspace, stream=s, side_stream=side)
+        rec("backward")
+
     with torch.cuda.stream(s):
         for i in range(args.warmup):
             flush_l2()
-            step(i, s)
+            step(i, lambda name: None)
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    marks = [[] for _ in range(args.steps)]  # (phase, event) per step, in order
+
+    def recorder(i):
+        def rec(name):
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(s)
+            marks[i].append((name, ev))
+        return rec
+
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    # kernels of one step: the fused forward, and for training the backward's
-    # interaction, key fill and expansion, 3 per radix pass, 2 for the row updates
-    per_step = 1 + ((5 + 3 * sort_passes(w)) if w.train else 0)
+    # kernels of one step (our library's launches)
+    per_step = launches_per_step(args, w, plan if args.shards > 1 else None)
     launches = 0
     with ClockSampler(local) as clk, torch.cuda.stream(s):
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush_l2()                         # evict L2 (outside the timed events)
             starts[i].record(s)
-            step(args.warmup + i, s, mids[i])
+            step(args.warmup + i, recorder(i))
             launches += per_step
-            ends[i].record(s)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     if world > 1:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    total_ms = max_over_ranks(total_ms, world)
+    step_ms = [a.elapsed_time(m[-1][1]) for a, m in zip(starts, marks)]
+    phase_ms = {}
+    for a, m in zip(starts, marks):
+        prev = a
+        for name, ev in m:
+            phase_ms.setdefault(name, []).append(prev.elapsed_time(ev))
+            prev = ev
+    total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     value = w.B * world * args.steps / (total_ms / 1e3)
     peak, src = peaks()
 
-    if not w.train:
-        # roofline of the fused kernel (the step is that one kernel)
-        alg = statistics.mean(algorithmic_bytes(w, b) for b in batches)
-        kernel_ms = statistics.mean(step_ms)
-        achieved = alg / (kernel_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic_for(args.workload),
-                "kernel": forward_kernel_name(w), "peak_source": f"{src} (hbm_gbs, burst copy)",
-                "algorithmic_bytes_per_launch": int(alg), "frac_of_nominal_8000": round(achieved / 8000.0, 4),
-                "median_launch_ms": round(statistics.median(step_ms), 4)}
-        effective = achieved
-    else:
-        tb = [train_bytes(w, b) for b in batches]
-        fwd_ms = [a.elapsed_time(m) for a, m in zip(starts, mids)]
-        bwd_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
-        fwd_b = statistics.mean(t["forward"] for t in tb)
-        bwd_b = statistics.mean(t["backward"] for t in tb)
-        tot_b = fwd_b + bwd_b
-        effective = tot_b / (statistics.mean(step_ms) / 1e3) / 1e9
-        fwd_gbs = fwd_b / (statistics.mean(fwd_ms) / 1e3) / 1e9
-        bwd_gbs = bwd_b / (statistics.mean(bwd_ms) / 1e3) / 1e9
-        dom = "backward" if statistics.mean(bwd_ms) >= statistics.mean(fwd_ms) else "forward"
-        ach = bwd_gbs if dom == "backward" else fwd_gbs
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                "traffic": traffic_for(args.workload),
-                "kernel": ("dlrm_sparse_bwd_adagrad kernels (interaction backward, keys, radix sort, row updates)"
-                           if dom == "backward" else forward_kernel_name(w)),
-                "peak_source": f"{src} (hbm_gbs, burst copy)",
-                "algorithmic_bytes_per_launch": int(bwd_b if dom == "backward" else fwd_b),
-                "phases": {"forward_ms": round(statistics.mean(fwd_ms), 4), "forward_gbs": round(fwd_gbs, 1),
-                           "forward_bytes": int(fwd_b), "backward_ms": round(statistics.mean(bwd_ms), 4),
-                           "backward_gbs": round(bwd_gbs, 1), "backward_bytes": int(bwd_b),
-                           "touched_rows": int(statistics.mean(t["touched_rows"] for t in tb))},
-                "step_effective_gbs": round(effective, 1), "step_frac": round(effective / peak, 4)}
+    pb = [phase_bytes(args, w, b) for b in batches]
+    phases = {}
+    for name, ms in phase_ms.items():
+        by = statistics.mean(p[name] for p in pb)
+        gbs = by / (statistics.mean(ms) / 1e3) / 1e9
+        phases[name] = {"ms": round(statistics.mean(ms), 4), "bytes": int(by), "gbs": round(gbs, 1),
+                        "frac": round(gbs / peak, 4)}
+    dom = max(phases, key=lambda n: phases[n]["ms"])
+    step_bytes = sum(p["bytes"] for p in phases.values())
+    effective = step_bytes / (statistics.mean(step_ms) / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": phases[dom]["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": phases[dom]["frac"], "traffic": traffic_for(args.workload) if phase_is_traced(args, dom) else None,
+            "kernel": kernel_of_phase(args, w, dom), "phase": dom, "peak_source": f"{src} (hbm_gbs, burst copy)",
+            "algorithmic_bytes_per_launch": phases[dom]["bytes"], "frac_of_nominal_8000":
+            round(phases[dom]["gbs"] / 8000.0, 4), "median_launch_ms": round(statistics.median(phase_ms[dom]), 4),
+            "phases": phases, "step_effective_gbs": round(effective, 1), "step_frac": round(effective / peak, 4)}
+    if w.train and args.shards == 1:
+        tbs = [train_bytes(w, b, args.rule) for b in batches]
+        lookup_model = statistics.mean(t["backward_per_lookup"] for t in tbs)
+        bw = lookup_model / (statistics.mean(phase_ms["backward"]) / 1e3) / 1e9
+        roof["backward_per_lookup_model"] = {"bytes": int(lookup_model), "gbs": round(bw, 1),
+                                             "frac": round(bw / peak, 4)}
+        roof["touched_rows"] = int(statistics.mean(t["touched_rows"] for t in tbs))
 
     e2e = None
-    if not args.no_e2e:
-        e2e = (run_e2e_train(args, w, tables, batches, dev, dl, torch, world) if w.train
+    if not args.no_e2e and args.shards == 1 and not args.hash:
+        e2e = (run_e2e_train(args, w, tables, batches, dev, dl, torch, world, side) if w.train
                else run_e2e(args, w, tables, batches, dev, dl, torch, world))
+        e2e["host_link"] = host_link(torch, dev, e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
 
     cpu = None
     if rank == 0 and not args.no_cpu and world == 1:
-        cpu = oracle_baseline(w, batches[0], args.cpu_seconds)
+        cpu = oracle_baseline(w, batches[0], args.cpu_seconds, args.rule)
 
     if rank == 0:
         line = {"metric": TRAIN_METRIC if w.train else METRIC, "value": round(value, 1), "unit": "samples/s",
@@ -514,6 +633,84 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+def passes_for_rows(total_rows: int) -> int:
+    bits = 1
+    while (1 << bits) <= total_rows:
+        bits += 1
+    return (bits + 8) // 9
+
+
+def launches_per_step(args, w, plan=None) -> int:
+    """Kernels of this library one step launches."""
+    n = 1 if args.hash else 0
+    if plan is not None:
+        G = plan.G
+        n += G + 1 + plan.H  # lookup per table shard, exchange, interaction per sample shard
+        if w.train:
+            # interaction backward per sample shard, exchange, per table shard: key fill and expansion,
+            # 3 per radix pass over that shard's rows, 2 row updates (+ the bag-length scaling in mean mode)
+            n += plan.H + 1
+            for g in range(G):
+                rows = sum(w.num_rows[t] for t in plan.tables_of(g))
+                n += 4 + 3 * passes_for_rows(rows) + (1 if w.mode == "mean" else 0)
+        return n
+    bwd = 5 + 3 * sort_passes(w)  # interaction backward, key fill and expansion, 3 per radix pass, 2 row updates
+    return n + 1 + (bwd if w.train else 0)
+
+
+def phase_is_traced(args, phase) -> bool:
+    """profiles/traffic.json holds DRAM bytes of the plain forward kernel and of the plain backward."""
+    return args.shards == 1 and not args.hash and phase in ("forward", "backward")
+
+
+def kernel_of_phase(args, w, phase) -> str:
+    return {"forward": forward_kernel_name(w),
+            "backward": "dlrm_sparse_bwd_update kernels (interaction backward, keys, radix sort, row updates; "
+                        f"{args.rule})",
+            "hash": "hash_kernel (raw ID mod V_t)",
+            "lookup": "embedding-bag forward per table shard",
+            "exchange": "exchange_kernel (all-to-all of the pooled vectors between logical shards)",
+            "interaction": "interaction forward per sample shard (forward_tc_kernel, pooled inputs)",
+            "interaction_bwd": "interact_bwd_kernel per sample shard",
+            "exchange_bwd": "exchange_kernel (pooled gradients back to the table owners)",
+            "update": f"embedding-bag backward per table shard (keys, radix sort, row updates; {args.rule})"}[phase]
+
+
+def host_link(torch, dev, h2d_bytes, d2h_bytes, reps=5):
+    """The host link alone: bare pinned cudaMemcpyAsync copies of one step's input and output bytes, each
+    direction timed on its own (CUDA events, best of `reps`), and both directions at once."""
+    hi = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    di = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    do = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    ho = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            el = time.perf_counter() - t0
+            best = el if best is None else min(best, el)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            di.copy_(hi, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            ho.copy_(do, non_blocking=True)
+
+    t_in, t_out = timed(h2d), timed(d2h)
+    t_both = timed(lambda: (h2d(), d2h()))
+    return {"h2d_gbs": round(h2d_bytes / t_in / 1e9, 1), "d2h_gbs": round(d2h_bytes / t_out / 1e9, 1),
+            "both_ms": round(t_both * 1e3, 4), "h2d_ms": round(t_in * 1e3, 4), "d2h_ms": round(t_out * 1e3, 4),
+            "how": "bare pinned copies of one step's bytes, wall clock around synchronised copies, best of 5"}
+
+
 def forward_kernel_name(w):
     """Which forward kernel the library picks for this workload (mirrors its dispatch)."""
     mean_len = (w.bag_max + w.bag_min) / 2
@@ -524,7 +721,7 @@ def forward_kernel_name(w):
             + (", multi-lookup bags)" if mean_len > 1.25 else ")"))
 
 
-def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):
+def run_e2e_train(args, w, tables, batches, dev, dl, torch, world, side):
     """Training steps fed from pinned host memory: indices, offsets, dense and
     grad_out copied in on a copy stream (the next step's copies overlap this
     step's kernels), grad_dense copied back, all inside the timed region."""
@@ -532,14 +729,14 @@ def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):
             for b in batches]
     max_nnz = max(b.nnz for b in batches)
     comp, copy = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    side = torch.cuda.Stream(device=dev, priority=-100)
     stages = []
     for _ in range(2):
         stages.append((torch.empty(max_nnz, dtype=torch.int32, device=dev),
                        torch.empty(w.T * w.B + 1, dtype=torch.int32, device=dev),
                        torch.empty((w.B, w.D), dtype=torch.float32, device=dev),
                        torch.empty((w.B, w.out_width), dtype=torch.float32, device=dev)))
-    accum = [torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+    accum = ([torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+             if args.rule == "adagrad" else None)
     pooled = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device=dev)
     out = torch.empty((w.B, w.out_width), dtype=torch.float32, device=dev)
     gd = torch.empty((w.B, w.D), dtype=torch.float32, device=dev)
@@ -571,8 +768,8 @@ def run_e2e_train(args, w, tables, batches, dev, dl, torch, world):
         di, do, dx, dg = stages[k]
         comp.wait_event(copied[k])
         dl.dlrm_sparse_fwd(tables, di[:hi.numel()], do, dx, w.mode, out=out, pooled_save=pooled, stream=comp)
-        dl.dlrm_sparse_bwd_adagrad(tables, accum, di[:hi.numel()], do, dx, pooled, dg, w.lr, w.eps, w.mode,
-                                   grad_dense=gd, workspace=ws, stream=comp, side_stream=side)
+        dl.dlrm_sparse_bwd_update(tables, di[:hi.numel()], do, dx, pooled, dg, args.rule, w.lr, w.eps, accum,
+                                  w.mode, grad_dense=gd, workspace=ws, stream=comp, side_stream=side)
         with torch.cuda.stream(comp):
             gd_host[k].copy_(gd, non_blocking=True)
         ev = torch.cuda.Event()
@@ -658,6 +855,13 @@ def main():
     if args.uniform:
         w.index_dist = "uniform"
         w.name += " [uniform indices]"
+    if w.train and args.rule != "adagrad":
+        w.name = w.name.replace("row-wise Adagrad", "plain SGD")
+        w.name += f" [{args.rule}]" if "plain SGD" not in w.name else ""
+    if args.shards > 1:
+        w.name += f" [tables over {args.shards} logical shards]"
+    if args.hash:
+        w.name += " [raw IDs hashed in the step]"
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -220,9 +220,11 @@ class ShardedSparse:
     def _exchange(self, to_sample: int, by_table, by_sample, stream=None):
         pooled_exchange(self._c, by_table, by_sample, to_sample, stream)
 
-    def forward(self, shard_bags, dense, mode="sum", out=None, stream=None):
+    def forward(self, shard_bags, dense, mode="sum", out=None, stream=None, after=None):
         """shard_bags[g] = (indices_g, offsets_g) on the device (split_bags); dense [B, D].  Returns out
-        [B, D + N(N-1)/2]; the sample shards' pooled vectors stay in self.by_sample for the backward."""
+        [B, D + N(N-1)/2]; the sample shards' pooled vectors stay in self.by_sample for the backward.
+        after(name), if given, is called once each phase ("lookup", "exchange", "interaction") is queued
+        (a caller records events there to time the phases)."""
         from . import dlrm_embbag_fwd, dlrm_interact_fwd
         p = self.plan
         N = p.T + 1
@@ -232,34 +234,60 @@ class ShardedSparse:
             if self.shard_tables[g] is not None:
                 idx, off = shard_bags[g]
                 dlrm_embbag_fwd(self.shard_tables[g], idx, off, mode, pooled=self.by_table[g], stream=stream)
+        if after:
+            after("lookup")
         self._exchange(1, self.by_table, self.by_sample, stream)
+        if after:
+            after("exchange")
         for h in range(p.H):
             lo, hi = p.samples_of(h)
             if hi > lo:
                 dlrm_interact_fwd(dense[lo:hi], self.by_sample[h], out=out[lo:hi], stream=stream)
+        if after:
+            after("interaction")
         return out
 
     def backward(self, shard_bags, dense, grad_out, rule, lr, eps=0.0, accum=None, mode="sum", grad_dense=None,
-                 stream=None):
+                 stream=None, side_stream=None, after=None):
         """After forward(): interaction backward per sample shard, reverse exchange, row update per table
-        shard (accum: the T global accumulators for Adagrad).  Returns grad_dense [B, D]."""
+        shard (accum: the T global accumulators for Adagrad).  Returns grad_dense [B, D].  after(name) as
+        in forward, for "interaction_bwd", "exchange_bwd", "update"."""
         from . import dlrm_embbag_bwd_update, dlrm_interact_bwd
         p = self.plan
         if grad_dense is None:
             grad_dense = self.torch.empty((p.B, p.D), dtype=self.torch.float32, device=self.dev)
-        grad_sample = [self.torch.empty_like(x) for x in self.by_sample]
+        if not hasattr(self, "grad_sample"):
+            self.grad_sample = [self.torch.empty_like(x) for x in self.by_sample]
+            self.grad_table = [self.torch.empty_like(x) for x in self.by_table]
         for h in range(p.H):
             lo, hi = p.samples_of(h)
             if hi > lo:
                 dlrm_interact_bwd(dense[lo:hi], self.by_sample[h], grad_out[lo:hi], grad_dense=grad_dense[lo:hi],
-                                  grad_pooled=grad_sample[h], stream=stream)
-        grad_table = [self.torch.empty_like(x) for x in self.by_table]
-        self._exchange(0, grad_table, grad_sample, stream)
+                                  grad_pooled=self.grad_sample[h], stream=stream)
+        if after:
+            after("interaction_bwd")
+        self._exchange(0, self.grad_table, self.grad_sample, stream)
+        if after:
+            after("exchange_bwd")
         for g in range(p.G):
             if self.shard_tables[g] is None:
                 continue
             idx, off = shard_bags[g]
             acc = [accum[t] for t in p.tables_of(g)] if accum is not None else None
-            dlrm_embbag_bwd_update(self.shard_tables[g], idx, off, grad_table[g], rule, lr, eps, acc, mode,
-                                   stream=stream)
+            ws = self._workspace(g, idx, off, mode)
+            dlrm_embbag_bwd_update(self.shard_tables[g], idx, off, self.grad_table[g], rule, lr, eps, acc, mode,
+                                   workspace=ws, stream=stream, side_stream=side_stream)
+        if after:
+            after("update")
         return grad_dense
+
+    def _workspace(self, g, idx, off, mode):
+        """A workspace per table shard, grown when a batch needs more (allocated outside any timed step
+        once the largest batch has been seen)."""
+        from . import dlrm_embbag_bwd_workspace_size
+        if not hasattr(self, "_ws"):
+            self._ws = [None] * self.plan.G
+        need = max(dlrm_embbag_bwd_workspace_size(self.shard_tables[g], idx, off, mode), 16)
+        if self._ws[g] is None or self._ws[g].numel() < need:
+            self._ws[g] = self.torch.empty(need, dtype=self.torch.uint8, device=self.dev)
+        return self._ws[g]

@@ -66,7 +66,13 @@ class Oracle:
         lib.oracle_embbag_bwd_update.restype = _I
         lib.oracle_hash_indices.argtypes = [_I, _I64, _I64, _P, _P, _P, _P]
         lib.oracle_hash_indices.restype = _I
+        lib.oracle_set_threads.argtypes = [_I]
+        lib.oracle_set_threads.restype = _I
         self.lib = lib
+
+    def set_threads(self, n: int) -> int:
+        """Threads of the oracle's OpenMP loops (arithmetic unchanged); returns the count in effect."""
+        return self.lib.oracle_set_threads(int(n))
 
     # -- helpers ---------------------------------------------------------
     @staticmethod

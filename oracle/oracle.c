@@ -52,6 +52,7 @@
  *     unsigned 64-bit integer, modulo V_t.
  */
 #include <math.h>
+#include <omp.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -69,6 +70,16 @@
 
 #define ORACLE_ADAGRAD 0
 #define ORACLE_SGD 1
+
+/* Threads of the OpenMP loops over independent samples or tables (n >= 1);
+ * returns the count now in effect.  Changes no arithmetic: each sample's and
+ * each table's loops run the same way on any number of threads. */
+int oracle_set_threads(int n)
+{
+    if (n >= 1)
+        omp_set_num_threads(n);
+    return omp_get_max_threads();
+}
 
 /* One table element widened to double.  bf16 is the top half of an fp32
  * pattern, so widening is exact. */

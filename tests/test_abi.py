@@ -135,3 +135,32 @@ def _load_missing(tmp_path):
         return dl.load_library(str(tmp_path / "missing.so"))
     finally:
         dl._lib = saved
+
+
+def _build_c_smoke(tmp_path):
+    import subprocess
+    exe = str(tmp_path / "c_abi_smoke")
+    libdir = os.path.dirname(dlbuild.LIB)
+    cmd = ["gcc", "-std=c99", "-Wall", "-Werror", "-o", exe, os.path.join(ROOT, "tests", "c_abi_smoke.c"),
+           "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include", "-L", libdir, "-ldlrm_sparse",
+           f"-Wl,-rpath,{libdir}", "-L", "/usr/local/cuda/lib64", "-lcudart", "-Wl,-rpath,/usr/local/cuda/lib64"]
+    subprocess.run(cmd, check=True)
+    return exe
+
+
+def test_plain_c_consumer_host_checks(lib, tmp_path):
+    """The header compiles as C99 with warnings as errors and a C program linked against the library
+    (no Python) gets the declared host-side behaviour."""
+    import subprocess
+    r = subprocess.run([_build_c_smoke(tmp_path)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert "c abi smoke ok" in r.stdout
+
+
+@pytest.mark.gpu
+def test_plain_c_consumer_device_forwards(lib, tmp_path):
+    """The C program's identity-table forwards on the device: exact closed-form outputs."""
+    import subprocess
+    r = subprocess.run([_build_c_smoke(tmp_path), "--gpu"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert "with device forwards" in r.stdout
