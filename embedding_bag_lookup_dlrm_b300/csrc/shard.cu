@@ -14,9 +14,13 @@
 // devices (each receiving, from every table shard, the rows of its own
 // samples) it is the local unpack, with one sample shard.
 //
-// HBM-bound: each row is read once and written once.  One warp per row, the
-// rows in sample-major order so that consecutive warps write (or read)
-// consecutive rows of a by-sample buffer.
+// HBM-bound: each row is read once and written once.  A warp moves one sample
+// at a time: its T rows are one contiguous block of the by-sample buffer, and
+// row t of it sits in the by-table buffer of t's owner at sample stride
+// T_g * D.  The block stages, per table, that source (or destination) base and
+// stride in shared memory; a lane then walks the sample's T*D/4 16-byte chunks
+// (consecutive lanes, consecutive chunks) with kUnroll loads in flight before
+// the matching stores.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,31 +28,58 @@ namespace dlrm {
 namespace {
 
 constexpr int kExThreads = 256;
+constexpr int kUnroll = 8;
 
-__global__ void __launch_bounds__(kExThreads) exchange_kernel(const __grid_constant__ ExchangeArgs a)
+__global__ void __launch_bounds__(kExThreads) exchange_kernel(const __grid_constant__ ExchangeArgs a, int chunk_shift)
 {
+    __shared__ float* tab_base[DLRM_MAX_TABLES];   // by_table[g] + slot(t) * D
+    __shared__ int64_t tab_stride[DLRM_MAX_TABLES];  // T_g * D: elements between samples
+    __shared__ int64_t start[DLRM_MAX_SHARDS + 1];
+    for (int t = threadIdx.x; t < a.T; t += kExThreads) {
+        const int g = a.table_shard[t];
+        tab_base[t] = a.by_table[g] + static_cast<int64_t>(a.table_slot[t]) * a.D;
+        tab_stride[t] = static_cast<int64_t>(a.shard_tables[g]) * a.D;
+    }
+    for (int h = threadIdx.x; h <= a.H; h += kExThreads) start[h] = a.sample_start[h];
+    __syncthreads();
+
     const int lane = threadIdx.x % kWarp;
+    const int chunk_mask = (1 << chunk_shift) - 1;  // 16-byte chunks per row: D / 4, a power of two
+    const int n = a.T << chunk_shift;                // chunks per sample
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (kExThreads / kWarp);
-    const int64_t rows = a.batch * a.T;
-    const int chunks = a.D / 4;
-    for (int64_t r = blockIdx.x * int64_t{kExThreads / kWarp} + threadIdx.x / kWarp; r < rows; r += warps) {
-        const int64_t b = r / a.T;
-        const int t = static_cast<int>(r - b * a.T);
-        int lo = 0, hi = a.H - 1;  // the sample shard of b: the last h with sample_start[h] <= b
+    for (int64_t b = blockIdx.x * int64_t{kExThreads / kWarp} + threadIdx.x / kWarp; b < a.batch; b += warps) {
+        int lo = 0, hi = a.H - 1;  // the sample shard of b: the last h with start[h] <= b
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (a.sample_start[mid] <= b)
+            if (start[mid] <= b)
                 lo = mid;
             else
                 hi = mid - 1;
         }
-        const int g = a.table_shard[t];
-        float4* tp = reinterpret_cast<float4*>(a.by_table[g] + (b * a.shard_tables[g] + a.table_slot[t]) * a.D);
-        float4* sp = reinterpret_cast<float4*>(a.by_sample[lo] + ((b - a.sample_start[lo]) * a.T + t) * a.D);
-        if (a.to_sample) {
-            for (int c = lane; c < chunks; c += kWarp) sp[c] = tp[c];
-        } else {
-            for (int c = lane; c < chunks; c += kWarp) tp[c] = sp[c];
+        float4* sample_side = reinterpret_cast<float4*>(a.by_sample[lo] + (b - start[lo]) * a.T * a.D);
+        for (int e0 = 0; e0 < n; e0 += kUnroll * kWarp) {
+            float4 v[kUnroll];
+            float4* far[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int e = e0 + u * kWarp + lane;
+                far[u] = nullptr;
+                if (e < n) {
+                    const int t = e >> chunk_shift;
+                    far[u] = reinterpret_cast<float4*>(tab_base[t] + b * tab_stride[t]) + (e & chunk_mask);
+                    v[u] = a.to_sample ? *far[u] : sample_side[e];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int e = e0 + u * kWarp + lane;
+                if (e < n) {
+                    if (a.to_sample)
+                        sample_side[e] = v[u];
+                    else
+                        *far[u] = v[u];
+                }
+            }
         }
     }
 }
@@ -57,13 +88,15 @@ __global__ void __launch_bounds__(kExThreads) exchange_kernel(const __grid_const
 
 dlrm_status launch_exchange(const ExchangeArgs& a, cudaStream_t s)
 {
-    const int64_t rows = a.batch * a.T;
-    if (rows == 0) return DLRM_OK;
+    if (a.batch == 0) return DLRM_OK;
     const int sms = sm_count();
     if (sms < 1) return DLRM_ERR_CUDA;
-    const int64_t want = (rows + kExThreads / kWarp - 1) / (kExThreads / kWarp);
+    int chunk_shift = 0;
+    while ((1 << chunk_shift) < a.D / 4) ++chunk_shift;
+    if ((1 << chunk_shift) != a.D / 4) return DLRM_ERR_UNSUPPORTED;
+    const int64_t want = (a.batch + kExThreads / kWarp - 1) / (kExThreads / kWarp);
     const int64_t cap = static_cast<int64_t>(sms) * 8;
-    exchange_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kExThreads, 0, s>>>(a);
+    exchange_kernel<<<static_cast<unsigned>(want < cap ? want : cap), kExThreads, 0, s>>>(a, chunk_shift);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 

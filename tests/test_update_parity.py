@@ -182,3 +182,26 @@ def test_hashed_ids_feed_the_forward(orc):
     torch.cuda.synchronize()
     assert st == 0 and ref["status"] == 0
     assert_close(out.cpu().numpy(), ref["out"], ref["out_abs"], TOL_INTERACT, "hashed forward")
+
+
+@pytest.mark.parametrize("itype", ["i32", "i64"])
+def test_hash_indices_unaligned_buffers(itype, orc):
+    """IDs and rows 8 bytes off a 16-byte boundary: the one-lookup-per-thread path of the kernel."""
+    T, B = 5, 777
+    rng = np.random.default_rng(620)
+    V = [3, 1000, 65537, 1 << 30, 17]
+    L = rng.integers(0, 7, size=T * B)
+    off = np.zeros(T * B + 1, np.int64)
+    np.cumsum(L, out=off[1:])
+    raw = rng.integers(np.iinfo(np.int64).min, np.iinfo(np.int64).max, size=int(off[-1]), dtype=np.int64)
+    ref, st = orc.hash_indices(V, raw, off, B)
+    buf = torch.empty(raw.size + 1, dtype=torch.int64, device="cuda")
+    buf[1:] = torch.from_numpy(raw).cuda()
+    dt = torch.int32 if itype == "i32" else torch.int64
+    rows_buf = torch.empty(raw.size + 2, dtype=dt, device="cuda")
+    rows = rows_buf[2:] if itype == "i32" else rows_buf[1:-1]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dl.dlrm_hash_indices(V, buf[1:], dev_index(off, itype), rows=rows, status=status)
+    torch.cuda.synchronize()
+    assert st == 0 and status.item() == 0
+    assert np.array_equal(rows.cpu().numpy().astype(np.int64), ref)
