@@ -59,6 +59,8 @@ def parse():
     p.add_argument("--shards", type=int, default=1,
                    help="G > 1: table-wise model parallelism over G logical shards on this device (the "
                         "embedding-bag lookup per table shard, the exchange, the interaction per sample shard)")
+    p.add_argument("--op", choices=["fused", "embbag"], default="fused",
+                   help="embbag: time the embedding-bag lookup alone (pooled vectors written to HBM)")
     p.add_argument("--hash", action="store_true",
                    help="the bags arrive as raw 64-bit IDs: the hashing pre-pass (ID mod V_t) runs in each step")
     return p.parse_args()
@@ -409,7 +411,9 @@ def config_of(w, args):
             + (f"; tables split over {args.shards} logical shards on each device (table-wise model parallel, "
                "all-to-all by the exchange kernel)" if args.shards > 1 else ""),
             **({"update_rule": args.rule} if w.train else {}),
-            **({"indices": "raw 64-bit IDs, hashed to rows (ID mod V_t) inside each step"} if args.hash else {})}
+            **({"indices": "raw 64-bit IDs, hashed to rows (ID mod V_t) inside each step"} if args.hash else {}),
+            **({"op": "embedding-bag lookup alone (dlrm_embbag_fwd), pooled vectors written"}
+               if args.op == "embbag" else {})}
 
 
 # ---------------------------------------------------------------------------
@@ -434,6 +438,9 @@ def phase_bytes(args, w: gen.Workload, b: gen.Batch) -> dict:
             ph["interaction_bwd"] = out + x + BTD + x + BTD
             ph["exchange_bwd"] = exchange_bytes(w)
             ph["update"] = tb["backward"] - ph["interaction_bwd"]
+        return ph
+    if args.op == "embbag":
+        ph["lookup"] = rows + csr + BTD
         return ph
     if w.train:
         tb = train_bytes(w, b, args.rule)
@@ -473,6 +480,8 @@ def run_ours(args, w):
     dl.load_library()
     if args.hash and args.shards > 1:
         raise SystemExit("--hash and --shards together are not a configuration of this bench")
+    if args.op == "embbag" and args.shards > 1:
+        raise SystemExit("--op embbag times the lookup of an unsharded workload")
 
     # tables: filled on the device by the seeded generator
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -495,6 +504,8 @@ def run_ours(args, w):
         flush.zero_()
         drain.sum()
 
+    if args.op == "embbag":
+        pooled_out = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device=dev)
     if args.hash:
         raws = [torch.from_numpy(raw_ids_for(w, b, 77 + i)).to(dev) for i, b in enumerate(batches)]
         hashed = torch.empty(max(b.nnz for b in batches), dtype=torch.int32, device=dev)
@@ -531,6 +542,10 @@ def run_ours(args, w):
             if w.train:
                 sharded.backward(shard_bags[k], x, grads[k], args.rule, w.lr, w.eps, accum, w.mode,
                                  grad_dense=grad_dense, stream=s, side_stream=side, after=rec)
+            return
+        if args.op == "embbag":
+            dl.dlrm_embbag_fwd(tables, idx, off, w.mode, pooled=pooled_out, stream=s)
+            rec("lookup")
             return
         if not w.train:
             dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, stream=s)
@@ -611,7 +626,7 @@ def run_ours(args, w):
         roof["touched_rows"] = int(statistics.mean(t["touched_rows"] for t in tbs))
 
     e2e = None
-    if not args.no_e2e and args.shards == 1 and not args.hash:
+    if not args.no_e2e and args.shards == 1 and not args.hash and args.op == "fused":
         e2e = (run_e2e_train(args, w, tables, batches, dev, dl, torch, world, side) if w.train
                else run_e2e(args, w, tables, batches, dev, dl, torch, world))
         e2e["host_link"] = host_link(torch, dev, e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
@@ -655,7 +670,7 @@ def launches_per_step(args, w, plan=None) -> int:
                 n += 4 + 3 * passes_for_rows(rows) + (1 if w.mode == "mean" else 0)
         return n
     bwd = 5 + 3 * sort_passes(w)  # interaction backward, key fill and expansion, 3 per radix pass, 2 row updates
-    return n + 1 + (bwd if w.train else 0)
+    return n + 1 + (bwd if w.train and args.op == "fused" else 0)
 
 
 def phase_is_traced(args, phase) -> bool:
@@ -668,7 +683,8 @@ def kernel_of_phase(args, w, phase) -> str:
             "backward": "dlrm_sparse_bwd_update kernels (interaction backward, keys, radix sort, row updates; "
                         f"{args.rule})",
             "hash": "hash_kernel (raw ID mod V_t)",
-            "lookup": "embedding-bag forward per table shard",
+            "lookup": "embbag_kernel (embedding-bag lookup, a lane group per bag"
+                      + (", once per table shard)" if args.shards > 1 else ")"),
             "exchange": "exchange_kernel (all-to-all of the pooled vectors between logical shards)",
             "interaction": "interaction forward per sample shard (forward_tc_kernel, pooled inputs)",
             "interaction_bwd": "interact_bwd_kernel per sample shard",
@@ -862,6 +878,9 @@ def main():
         w.name += f" [tables over {args.shards} logical shards]"
     if args.hash:
         w.name += " [raw IDs hashed in the step]"
+    if args.op == "embbag":
+        w.name += " [embedding-bag lookup alone]"
+        w.train = False  # a training workload's bags, looked up only
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -1,10 +1,11 @@
 // fwd.cu -- sm_103a kernels of the DLRM sparse forward.
 //
-// One kernel template covers the three forward entry points:
-//   kEmbbag    lookup + pooling           ("DLRM", robocikowo.com, "Forward pass" step (2);
-//                                          bags: "The embedding table is the model")
-//   kInteract  dot-product interaction    (same page, steps (3)-(4))
-//   kFused     both, pooled vectors kept in shared memory
+// One kernel template covers the fused forward and the interaction alone, for
+// the shapes the tensor-core kernel (fwd_tc.cu) does not take:
+//   kInteract  dot-product interaction    ("DLRM", robocikowo.com, "Forward pass" steps (3)-(4))
+//   kFused     lookup + pooling (step (2); bags: "The embedding table is the model") and the
+//              interaction, pooled vectors kept in shared memory
+// (the lookup alone, kEmbbag, runs in embbag.cu).
 //
 // Work unit: one sample.  A "group" of G warps owns one sample at a time and
 // stages its N = 1 + T vectors V (x first, then the pooled bags) as fp32 rows
@@ -418,7 +419,6 @@ dlrm_status dispatch_mode(int mode, const FwdArgs& a, cudaStream_t s)
 {
     const bool wide = wide_interaction(a.T);
     switch (mode) {
-        case kEmbbag: return launch_one<D, TE, TI, kEmbbag, 1>(a, s);
         case kFused:
             if (wide) return launch_one<D, TE, TI, kFused, 8>(a, s);
             return long_bags(a) ? launch_one<D, TE, TI, kFused, 2>(a, s) : launch_one<D, TE, TI, kFused, 1>(a, s);
@@ -443,6 +443,7 @@ dlrm_status dispatch_types(int mode, const FwdArgs& a, int dtype, int index_type
 
 dlrm_status launch_forward(int mode, const FwdArgs& a, int dim, int dtype, int index_type, cudaStream_t s)
 {
+    if (mode == kEmbbag) return launch_embbag(a, dim, dtype, index_type, s);
     if (forward_tc_supported(mode, dim, a.T, a.B, a.nnz)) return launch_forward_tc(mode, a, dim, dtype, index_type, s);
     switch (dim) {
         case 16: return dispatch_types<16>(mode, a, dtype, index_type, s);

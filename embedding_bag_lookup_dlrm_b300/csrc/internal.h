@@ -43,6 +43,9 @@ int kernel_registers(const void* kernel);
 dlrm_status launch_forward(int mode, const FwdArgs& args, int dim, int dtype, int index_type,
                            cudaStream_t stream);
 
+// The embedding-bag lookup alone (embbag.cu): a group of lanes per bag.
+dlrm_status launch_embbag(const FwdArgs& args, int dim, int dtype, int index_type, cudaStream_t stream);
+
 // The same forward with the interaction on the tensor cores (fwd_tc.cu):
 // fused and interaction modes, D in {64, 128}, N = T + 1 <= 128, bags of
 // at most two lookups on average.
