@@ -43,6 +43,12 @@ dlrm_status check_bags(const dlrm_bags* b, int32_t T)
 
 bool mode_ok(dlrm_pool_mode m) { return m == DLRM_POOL_SUM || m == DLRM_POOL_MEAN; }
 
+// The forward kernels count a warp's or a bag's lookups in 32-bit integers.
+dlrm_status check_forward_size(const dlrm_bags* b)
+{
+    return b->nnz > INT32_MAX ? DLRM_ERR_UNSUPPORTED : DLRM_OK;
+}
+
 void pack_forward(FwdArgs& a, const dlrm_tables* t, const dlrm_bags* b, dlrm_pool_mode mode)
 {
     memset(&a, 0, sizeof a);
@@ -85,6 +91,7 @@ dlrm_status dlrm_embbag_fwd(const dlrm_tables* tables, const dlrm_bags* bags, dl
     if (st != DLRM_OK) return st;
     if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
     if (!mode_ok(mode) || pooled == nullptr || !aligned16(pooled)) return DLRM_ERR_INVALID_ARG;
+    if ((st = check_forward_size(bags)) != DLRM_OK) return st;
     FwdArgs a;
     pack_forward(a, tables, bags, mode);
     a.pooled_out = pooled;
@@ -117,6 +124,7 @@ dlrm_status dlrm_sparse_fwd(const dlrm_tables* tables, const dlrm_bags* bags, dl
     if (st != DLRM_OK) return st;
     if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
     if (!mode_ok(mode) || dense == nullptr || out == nullptr || !aligned16(dense)) return DLRM_ERR_INVALID_ARG;
+    if ((st = check_forward_size(bags)) != DLRM_OK) return st;
     if (reinterpret_cast<uintptr_t>(out) & 3u) return DLRM_ERR_INVALID_ARG;
     if (pooled_save != nullptr && !aligned16(pooled_save)) return DLRM_ERR_INVALID_ARG;
     FwdArgs a;

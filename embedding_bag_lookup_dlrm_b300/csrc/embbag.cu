@@ -2,9 +2,9 @@
 // mean) of the rows of bag (t, b) ("DLRM", robocikowo.com, "Forward pass"
 // step (2); bags of several IDs: "The embedding table is the model").
 //
-// HBM-bound gather.  A group of P lanes owns one bag, P = the row's 16-byte
-// chunks (up to 32; D = 256 fp32 gives each lane two chunks), so a warp holds
-// 32 / P bags.  The group reads the bag's offsets once, its indices P at a
+// HBM-bound gather.  Rows of 128 bytes or more take the list form below.
+// Narrower rows: a group of P lanes owns one bag, P = the row's 16-byte
+// chunks, so a warp holds 32 / P bags.  The group reads the bag's offsets once, its indices P at a
 // time with one load per lane, and then walks the lookups eight at a time:
 // eight row loads in flight per lane before the adds.  Each sum is fp32 in
 // lookup order, starting from its first term (so a one-lookup fp32 bag is a
@@ -148,12 +148,220 @@ __global__ void __launch_bounds__(kBagThreads) embbag_kernel(const __grid_consta
     }
 }
 
+// The list form, for rows of at least 128 bytes.  A warp takes 32
+// consecutive bags (lane l reads bag l's offsets, so the loads coalesce),
+// flattens their lookups into one list, and walks it 32 lookups at a time:
+// lane j resolves lookup j of the step (its bag by a 5-step search over the
+// lanes' list ends, its index by one load, coalesced where the bags' ranges
+// are contiguous) while the next step's indices are already on their way.
+// The warp then streams the step's rows, kRows in flight, each lane holding
+// 1/32 of a row (16, 8 or 4 bytes; D = 256 fp32: two 16-byte pieces), adding
+// each into the running bag's sum in lookup order; a finished bag is written
+// once.  One-hot batches thus keep 32 bags' rows moving per warp instead of
+// one.
+constexpr int kRows = 16;
+
+template <int BYTES>
+struct Piece;
+template <>
+struct Piece<16> {
+    uint4 v;
+    __device__ __forceinline__ void load(const void* p) { v = __ldg(static_cast<const uint4*>(p)); }
+    __device__ __forceinline__ uint32_t w(int i) const { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+};
+template <>
+struct Piece<8> {
+    uint2 v;
+    __device__ __forceinline__ void load(const void* p) { v = __ldg(static_cast<const uint2*>(p)); }
+    __device__ __forceinline__ uint32_t w(int i) const { return i == 0 ? v.x : v.y; }
+};
+template <>
+struct Piece<4> {
+    uint32_t v;
+    __device__ __forceinline__ void load(const void* p) { v = __ldg(static_cast<const uint32_t*>(p)); }
+    __device__ __forceinline__ uint32_t w(int) const { return v; }
+};
+
+template <int D, typename TE>
+struct ListShape {
+    static constexpr int kRowBytes = D * static_cast<int>(sizeof(TE));
+    static constexpr int kLaneBytes = kRowBytes / kWarp;                 // 4 .. 32
+    static constexpr int kPieceBytes = kLaneBytes > 16 ? 16 : kLaneBytes;
+    static constexpr int kPieces = kLaneBytes / kPieceBytes;             // 1, or 2 (D = 256 fp32)
+    static constexpr int kElems = kPieceBytes / static_cast<int>(sizeof(TE));  // elements per piece
+};
+
+template <int D, typename TE, typename TI>
+__global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_constant__ FwdArgs a)
+{
+    using S = ListShape<D, TE>;
+    constexpr int NP = S::kPieces, NE = S::kElems, PB = S::kPieceBytes;
+    using PieceT = Piece<PB>;
+    const int lane = threadIdx.x % kWarp;
+    const int64_t nbags = static_cast<int64_t>(a.T) * a.B;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kBagThreads / kWarp);
+    const TI* off = static_cast<const TI*>(a.offsets);
+    const TI* ind = static_cast<const TI*>(a.indices);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const int64_t first = static_cast<int64_t>(__ldg(off));
+        const int64_t last = static_cast<int64_t>(__ldg(off + nbags));
+        if (first != 0 || last != a.nnz) flag_status(a.status, DLRM_ERR_BAD_OFFSETS);
+    }
+    for (int64_t w0 = (blockIdx.x * int64_t{kBagThreads / kWarp} + threadIdx.x / kWarp) * kWarp; w0 < nbags;
+         w0 += warps * kWarp) {
+        // lane l: bag w0 + l
+        const int64_t bag = w0 + lane;
+        const bool live = bag < nbags;
+        int64_t s0 = 0, s1 = 0;
+        if (live) {
+            s0 = static_cast<int64_t>(__ldg(off + bag));
+            s1 = static_cast<int64_t>(__ldg(off + bag + 1));
+            if (s0 < 0 || s1 < s0 || s1 > a.nnz) {
+                flag_status(a.status, DLRM_ERR_BAD_OFFSETS);  // treated as an empty bag
+                s0 = s1 = 0;
+            }
+        }
+        const int len = static_cast<int>(s1 - s0);
+        int incl = len;  // inclusive prefix of the bag lengths: the list end of each lane's bag
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
+        const int t_lane = live ? static_cast<int>(bag / a.B) : 0;
+
+        // lookup q of the list: its bag (lane) r and its index, or -1 when out of range
+        auto resolve = [&](int q, int& r, int64_t& idx) {
+            int at = 0;
+#pragma unroll
+            for (int bit = 16; bit > 0; bit >>= 1)
+                if (__shfl_sync(0xffffffffu, incl, at + bit - 1) <= q) at += bit;
+            r = at & (kWarp - 1);
+            const int beg = __shfl_sync(0xffffffffu, incl - len, r);
+            const int64_t st = __shfl_sync(0xffffffffu, s0, r);
+            idx = q < total ? static_cast<int64_t>(__ldg(ind + st + (q - beg))) : -1;
+        };
+
+        float acc[NP][NE];
+        int cur = -1;          // the bag (lane) being summed
+        bool started = false;  // it has received a valid row
+        auto finish = [&]() {  // write bag `cur` (all lanes)
+            if (cur < 0) return;
+            const int64_t bg = w0 + cur;
+            const int t = static_cast<int>(bg / a.B);
+            const int64_t b = bg - static_cast<int64_t>(t) * a.B;
+            const int L = __shfl_sync(0xffffffffu, len, cur);
+            float* dst = a.pooled_out + (b * a.T + t) * D;
+#pragma unroll
+            for (int k = 0; k < NP; ++k) {
+                float v[NE];
+#pragma unroll
+                for (int e = 0; e < NE; ++e) {
+                    float x = started ? acc[k][e] : 0.0f;
+                    if (a.mean && started) x = __fdiv_rn(x, static_cast<float>(L));
+                    v[e] = x;
+                }
+                float* d = dst + (lane * NP + k) * NE;
+                if constexpr (NE == 4) {
+                    *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
+                } else if constexpr (NE == 8) {
+                    reinterpret_cast<float4*>(d)[0] = make_float4(v[0], v[1], v[2], v[3]);
+                    reinterpret_cast<float4*>(d)[1] = make_float4(v[4], v[5], v[6], v[7]);
+                } else if constexpr (NE == 2) {
+                    *reinterpret_cast<float2*>(d) = make_float2(v[0], v[1]);
+                } else {
+                    d[0] = v[0];
+                }
+            }
+        };
+        // bags with no lookups never appear in the list: their zero rows first
+        for (uint32_t empty = __ballot_sync(0xffffffffu, live && len == 0); empty != 0; empty &= empty - 1) {
+            const int64_t bg = w0 + (__ffs(empty) - 1);
+            const int t = static_cast<int>(bg / a.B);
+            const int64_t b = bg - static_cast<int64_t>(t) * a.B;
+            float* dst = a.pooled_out + (b * a.T + t) * D;
+            for (int e = lane * 4; e < D; e += kWarp * 4)
+                *reinterpret_cast<float4*>(dst + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+
+        int r_next = 0;
+        int64_t i_next = -1;
+        if (total > 0) resolve(lane, r_next, i_next);
+        for (int q0 = 0; q0 < total; q0 += kWarp) {
+            const int r_me = r_next;
+            int64_t idx = i_next;
+            if (q0 + kWarp < total) resolve(q0 + kWarp + lane, r_next, i_next);  // the next step's indices
+            const int t_me = __shfl_sync(0xffffffffu, t_lane, r_me);
+            const char* src = nullptr;
+            if (q0 + lane < total) {
+                if (idx >= 0 && idx < a.num_rows[t_me])
+                    src = static_cast<const char*>(a.tables[t_me]) + static_cast<uint64_t>(idx) * S::kRowBytes;
+                else
+                    flag_status(a.status, DLRM_ERR_INDEX_OOB);  // contributes zero, still counts in L
+            }
+            const int n = min(kWarp, total - q0);
+#pragma unroll 1
+            for (int h = 0; h < n; h += kRows) {
+                PieceT raw[kRows][NP];
+#pragma unroll
+                for (int u = 0; u < kRows; ++u) {
+                    const char* p = reinterpret_cast<const char*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), (h + u) & (kWarp - 1)));
+                    if (h + u < n && p != nullptr) {
+#pragma unroll
+                        for (int k = 0; k < NP; ++k) raw[u][k].load(p + (lane * NP + k) * PB);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kRows; ++u) {
+                    const int ru = __shfl_sync(0xffffffffu, r_me, (h + u) & (kWarp - 1));
+                    const bool valid = __shfl_sync(0xffffffffu, src != nullptr, (h + u) & (kWarp - 1));
+                    if (h + u >= n) continue;
+                    if (ru != cur) {
+                        finish();
+                        cur = ru;
+                        started = false;
+                    }
+                    if (!valid) continue;
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) {
+                        float f[NE];
+                        if constexpr (sizeof(TE) == 4) {
+#pragma unroll
+                            for (int e = 0; e < NE; ++e) f[e] = __uint_as_float(raw[u][k].w(e));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < NE / 2; ++e) {
+                                const uint32_t x = raw[u][k].w(e);
+                                f[2 * e] = __uint_as_float(x << 16);
+                                f[2 * e + 1] = __uint_as_float(x & 0xffff0000u);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < NE; ++e) acc[k][e] = started ? acc[k][e] + f[e] : f[e];
+                    }
+                    started = true;
+                }
+            }
+        }
+        finish();
+    }
+}
+
 template <int D, typename TE, typename TI>
 dlrm_status launch_bags(const FwdArgs& a, cudaStream_t s)
 {
     using S = BagShape<D, TE>;
     const int sms = sm_count();
     if (sms < 1) return DLRM_ERR_CUDA;
+    if constexpr (D * sizeof(TE) >= 128) {
+        const int64_t nbags = static_cast<int64_t>(a.T) * a.B;
+        const int64_t want = (nbags + kBagThreads - 1) / kBagThreads;  // 32 bags per warp
+        const int64_t cap = static_cast<int64_t>(sms) * 8;
+        embbag_list_kernel<D, TE, TI><<<static_cast<unsigned>(want < cap ? want : cap), kBagThreads, 0, s>>>(a);
+        return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
+    }
     const int64_t nbags = static_cast<int64_t>(a.T) * a.B;
     const int64_t per_block = (kBagThreads / kWarp) * S::BPW;
     const int64_t want = (nbags + per_block - 1) / per_block;

@@ -89,7 +89,9 @@ typedef struct {
 } dlrm_tables;
 
 /* One batch of bags.  batch = B >= 1, nnz >= 0.  indices (device, nnz
- * entries) and offsets (device, T*B+1 entries) share index_type. */
+ * entries) and offsets (device, T*B+1 entries) share index_type.  The
+ * forward entry points take nnz <= 2^31 - 1 (DLRM_ERR_UNSUPPORTED above it;
+ * int32 indices imply it), the training step nnz < 2^32. */
 typedef struct {
     int64_t batch;
     int64_t nnz;
