@@ -192,10 +192,11 @@ struct ListShape {
 };
 
 template <int D, typename TE, typename TI>
-__global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_constant__ FwdArgs a)
+__global__ void __launch_bounds__(kBagThreads, 2) embbag_list_kernel(const __grid_constant__ FwdArgs a)
 {
     using S = ListShape<D, TE>;
     constexpr int NP = S::kPieces, NE = S::kElems, PB = S::kPieceBytes;
+    constexpr int R = NP > 1 ? kRows / 2 : kRows;  // rows in flight: the same bytes per lane for two-piece rows
     using PieceT = Piece<PB>;
     const int lane = threadIdx.x % kWarp;
     const int64_t nbags = static_cast<int64_t>(a.T) * a.B;
@@ -243,7 +244,13 @@ __global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_c
             idx = q < total ? static_cast<int64_t>(__ldg(ind + st + (q - beg))) : -1;
         };
 
+        // -0.0 is the additive identity that keeps every sum exact: -0.0 + x = x for every x, -0.0 included,
+        // so a sum seeded with it equals the sum that starts from its first term
         float acc[NP][NE];
+#pragma unroll
+        for (int k = 0; k < NP; ++k)
+#pragma unroll
+            for (int e = 0; e < NE; ++e) acc[k][e] = -0.0f;
         int cur = -1;          // the bag (lane) being summed
         bool started = false;  // it has received a valid row
         auto finish = [&]() {  // write bag `cur` (all lanes)
@@ -261,6 +268,7 @@ __global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_c
                     float x = started ? acc[k][e] : 0.0f;
                     if (a.mean && started) x = __fdiv_rn(x, static_cast<float>(L));
                     v[e] = x;
+                    acc[k][e] = -0.0f;  // seeded for the next bag
                 }
                 float* d = dst + (lane * NP + k) * NE;
                 if constexpr (NE == 4) {
@@ -300,12 +308,13 @@ __global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_c
                 else
                     flag_status(a.status, DLRM_ERR_INDEX_OOB);  // contributes zero, still counts in L
             }
+            const int tag = r_me | (src != nullptr ? 32 : 0);  // the lookup's bag and whether it has a row
             const int n = min(kWarp, total - q0);
 #pragma unroll 1
-            for (int h = 0; h < n; h += kRows) {
-                PieceT raw[kRows][NP];
+            for (int h = 0; h < n; h += R) {
+                PieceT raw[R][NP];
 #pragma unroll
-                for (int u = 0; u < kRows; ++u) {
+                for (int u = 0; u < R; ++u) {
                     const char* p = reinterpret_cast<const char*>(
                         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), (h + u) & (kWarp - 1)));
                     if (h + u < n && p != nullptr) {
@@ -314,9 +323,10 @@ __global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_c
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < kRows; ++u) {
-                    const int ru = __shfl_sync(0xffffffffu, r_me, (h + u) & (kWarp - 1));
-                    const bool valid = __shfl_sync(0xffffffffu, src != nullptr, (h + u) & (kWarp - 1));
+                for (int u = 0; u < R; ++u) {
+                    const int tu = __shfl_sync(0xffffffffu, tag, (h + u) & (kWarp - 1));
+                    const int ru = tu & 31;
+                    const bool valid = (tu & 32) != 0;
                     if (h + u >= n) continue;
                     if (ru != cur) {
                         finish();
@@ -338,8 +348,18 @@ __global__ void __launch_bounds__(kBagThreads) embbag_list_kernel(const __grid_c
                                 f[2 * e + 1] = __uint_as_float(x & 0xffff0000u);
                             }
                         }
+                        // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
+                        if constexpr (NE == 1) {
+                            acc[k][0] += f[0];
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < NE; ++e) acc[k][e] = started ? acc[k][e] + f[e] : f[e];
+                            for (int e = 0; e < NE; e += 2) {
+                                const float2 r2 = __fadd2_rn(make_float2(acc[k][e], acc[k][e + 1]),
+                                                             make_float2(f[e], f[e + 1]));
+                                acc[k][e] = r2.x;
+                                acc[k][e + 1] = r2.y;
+                            }
+                        }
                     }
                     started = true;
                 }
