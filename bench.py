@@ -541,7 +541,7 @@ def run_ours(args, w):
             sharded.forward(shard_bags[k], x, w.mode, out=out, stream=s, after=rec)
             if w.train:
                 sharded.backward(shard_bags[k], x, grads[k], args.rule, w.lr, w.eps, accum, w.mode,
-                                 grad_dense=grad_dense, stream=s, side_stream=side, after=rec)
+                                 grad_dense=grad_dense, stream=s, after=rec)
             return
         if args.op == "embbag":
             dl.dlrm_embbag_fwd(tables, idx, off, w.mode, pooled=pooled_out, stream=s)

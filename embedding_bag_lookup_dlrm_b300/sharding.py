@@ -248,7 +248,7 @@ class ShardedSparse:
         return out
 
     def backward(self, shard_bags, dense, grad_out, rule, lr, eps=0.0, accum=None, mode="sum", grad_dense=None,
-                 stream=None, side_stream=None, after=None):
+                 stream=None, after=None):
         """After forward(): interaction backward per sample shard, reverse exchange, row update per table
         shard (accum: the T global accumulators for Adagrad).  Returns grad_dense [B, D].  after(name) as
         in forward, for "interaction_bwd", "exchange_bwd", "update"."""
@@ -269,14 +269,29 @@ class ShardedSparse:
         self._exchange(0, self.grad_table, self.grad_sample, stream)
         if after:
             after("exchange_bwd")
+        # the table shards update disjoint tables from separate workspaces: on one device they run side by
+        # side, each on a stream of its own forked from the caller's stream and joined back to it
+        main = stream if stream is not None else self.torch.cuda.current_stream(self.dev)
+        if not hasattr(self, "_upd_streams"):
+            self._upd_streams = [self.torch.cuda.Stream(device=self.dev) for _ in range(p.G)]
+        fork = self.torch.cuda.Event()
+        fork.record(main)
+        joins = []
         for g in range(p.G):
             if self.shard_tables[g] is None:
                 continue
             idx, off = shard_bags[g]
             acc = [accum[t] for t in p.tables_of(g)] if accum is not None else None
             ws = self._workspace(g, idx, off, mode)
+            us = self._upd_streams[g]
+            us.wait_event(fork)
             dlrm_embbag_bwd_update(self.shard_tables[g], idx, off, self.grad_table[g], rule, lr, eps, acc, mode,
-                                   workspace=ws, stream=stream, side_stream=side_stream)
+                                   workspace=ws, stream=us)
+            ev = self.torch.cuda.Event()
+            ev.record(us)
+            joins.append(ev)
+        for ev in joins:
+            main.wait_event(ev)
         if after:
             after("update")
         return grad_dense
