@@ -146,20 +146,12 @@ def peaks():
     return 6400.0, "fallback"
 
 
-FORWARD_SOURCES = ("api.cu", "common.cuh", "fwd.cu", "fwd_tc.cu", "internal.h", "tc.cuh")
-BACKWARD_SOURCES = ("api.cu", "bwd.cu", "common.cuh", "internal.h")
+FORWARD_SOURCES = ("common.cuh", "fwd.cu", "fwd_tc.cu", "internal.h", "tc.cuh")
 
 
-def traffic_sources(workload: int):
-    """Source files of the kernels whose DRAM traffic a workload's line reports: the forward's, or for
-    the training workload the backward's (its line reports the backward kernels)."""
-    return list(BACKWARD_SOURCES if workload == 5 else FORWARD_SOURCES)
-
-
-def traffic_for(workload: int):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from a
-    committed one-pass ncu capture of the full-size workload, if it was taken on
-    the kernel sources as they are now (else None)."""
+def traffic_record(workload: int):
+    """The committed DRAM-traffic record of a workload's forward kernel (profiles/traffic.json), if it was
+    taken on the kernel sources as they are now (else None).  Records hold capped-table captures."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -167,9 +159,15 @@ def traffic_for(workload: int):
         d = json.load(open(path)).get(str(workload))
     except (ValueError, OSError):
         return None
-    if not d or d.get("sources_sha256") != sources_digest(traffic_sources(workload)):
+    if not d or d.get("sources_sha256") != sources_digest(FORWARD_SOURCES):
         return None
-    return d.get("dram_bytes_per_launch")
+    return d
+
+
+def traffic_for(workload: int):
+    """DRAM bytes per full-size launch, when a committed capture scales to it (else None)."""
+    d = traffic_record(workload)
+    return d.get("dram_bytes_per_launch") if d and d.get("scales_to_full_size") else None
 
 
 def sources_digest(files) -> str:
@@ -614,6 +612,10 @@ def run_ours(args, w):
     roof = {"bound": "hbm", "achieved": phases[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": phases[dom]["frac"], "traffic": traffic_for(args.workload) if phase_is_traced(args, dom) else None,
             "kernel": kernel_of_phase(args, w, dom), "phase": dom, "peak_source": f"{src} (hbm_gbs, burst copy)",
+            **({"traffic_capped_tables": {k: traffic_record(args.workload)[k] for k in
+                                          ("small_case", "small_case_uniform", "why_null")
+                                          if k in traffic_record(args.workload)}}
+               if phase_is_traced(args, dom) and traffic_record(args.workload) else {}),
             "algorithmic_bytes_per_launch": phases[dom]["bytes"], "frac_of_nominal_8000":
             round(phases[dom]["gbs"] / 8000.0, 4), "median_launch_ms": round(statistics.median(phase_ms[dom]), 4),
             "phases": phases, "step_effective_gbs": round(effective, 1), "step_frac": round(effective / peak, 4)}
@@ -674,8 +676,8 @@ def launches_per_step(args, w, plan=None) -> int:
 
 
 def phase_is_traced(args, phase) -> bool:
-    """profiles/traffic.json holds DRAM bytes of the plain forward kernel and of the plain backward."""
-    return args.shards == 1 and not args.hash and phase in ("forward", "backward")
+    """profiles/traffic.json holds DRAM bytes of the plain forward kernel."""
+    return args.shards == 1 and not args.uniform and args.max_rows == 0 and phase == "forward"
 
 
 def kernel_of_phase(args, w, phase) -> str:
