@@ -61,6 +61,10 @@ def parse():
                         "embedding-bag lookup per table shard, the exchange, the interaction per sample shard)")
     p.add_argument("--op", choices=["fused", "embbag"], default="fused",
                    help="embbag: time the embedding-bag lookup alone (pooled vectors written to HBM)")
+    p.add_argument("--tier", type=float, default=0.0,
+                   help="F > 0: the tables live in pinned host memory with a device cache of the fraction F of each "
+                        "table's rows (the hottest in separate history batches); each step stages its lookups, then "
+                        "runs the forward on the device buffers")
     p.add_argument("--hash", action="store_true",
                    help="the bags arrive as raw 64-bit IDs: the hashing pre-pass (ID mod V_t) runs in each step")
     return p.parse_args()
@@ -411,7 +415,9 @@ def config_of(w, args):
             **({"update_rule": args.rule} if w.train else {}),
             **({"indices": "raw 64-bit IDs, hashed to rows (ID mod V_t) inside each step"} if args.hash else {}),
             **({"op": "embedding-bag lookup alone (dlrm_embbag_fwd), pooled vectors written"}
-               if args.op == "embbag" else {})}
+               if args.op == "embbag" else {}),
+            **({"host_tier": f"tables in pinned host memory; device cache of {args.tier:g} of each table's rows, "
+                             "filled with the hottest rows of separate history batches"} if args.tier > 0 else {})}
 
 
 # ---------------------------------------------------------------------------
@@ -439,6 +445,10 @@ def phase_bytes(args, w: gen.Workload, b: gen.Batch) -> dict:
         return ph
     if args.op == "embbag":
         ph["lookup"] = rows + csr + BTD
+        return ph
+    if args.tier > 0:
+        ph["stage"] = b.nnz * 12 + b.tier_misses * w.D * w.elem_bytes * 2  # index, map, rewritten index; staged rows
+        ph["forward"] = algorithmic_bytes(w, b)
         return ph
     if w.train:
         tb = train_bytes(w, b, args.rule)
@@ -481,16 +491,38 @@ def run_ours(args, w):
     if args.op == "embbag" and args.shards > 1:
         raise SystemExit("--op embbag times the lookup of an unsharded workload")
 
-    # tables: filled on the device by the seeded generator
+    # tables: filled on the device by the seeded generator (copied to pinned host memory for the host tier)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     tabs = []
     stream = torch.cuda.current_stream()
     for t, V in enumerate(w.num_rows):
         x = torch.empty((V, w.D), dtype=dt, device=dev)
         gen.fill_table_device(x.data_ptr(), w.dtype, w.seed, t, 0, V, w.D, stream.cuda_stream)
+        if args.tier > 0:
+            h = torch.empty((V, w.D), dtype=dt).pin_memory()
+            h.copy_(x)
+            del x
+            x = h
         tabs.append(x)
-    tables = dl.Tables(tabs)
     batches = gen.make_batches(w, [rank * 1000 + i for i in range(N_ROTATE)])
+    if args.tier > 0:
+        # the cache: each table's hottest rows in separate history batches, not the timed ones
+        history = gen.make_batches(w, [rank * 1000 + 500 + i for i in range(N_ROTATE)])
+        cap = [max(0, int(args.tier * V)) for V in w.num_rows]
+        hot = dl.hot_rows([h.indices for h in history], [h.offsets for h in history], w.B, w.T, cap, w.num_rows)
+        stage_rows = [max(int(b.offsets[(t + 1) * w.B]) - int(b.offsets[t * w.B]) for b in batches)
+                      for t in range(w.T)]
+        tier = dl.TieredTables(tabs, cap, stage_rows, dev)
+        for t in range(w.T):
+            tier.fill(t, torch.from_numpy(hot[t]).to(dev))
+        for b in batches:  # lookups the cache misses (they are copied over the host link in the step)
+            off = b.offsets.astype(np.int64)
+            b.tier_misses = sum(int((~np.isin(b.indices[off[t * w.B]:off[(t + 1) * w.B]], hot[t])).sum())
+                                for t in range(w.T))
+        tables = tier.device_tables
+        staged = torch.empty(max(b.nnz for b in batches), dtype=torch.int32, device=dev)
+    else:
+        tables = dl.Tables(tabs)
     dev_batches = [tuple(torch.from_numpy(a).to(dev) for a in (b.indices, b.offsets, b.dense)) for b in batches]
     out = torch.empty((w.B, w.out_width), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -535,6 +567,9 @@ def run_ours(args, w):
         if args.hash:
             idx = dl.dlrm_hash_indices(w.num_rows, raws[k], off, rows=hashed[:raws[k].numel()], stream=s)
             rec("hash")
+        if args.tier > 0:
+            idx = tier.stage(idx, off, out=staged[:idx.numel()], stream=s)
+            rec("stage")
         if args.shards > 1:
             sharded.forward(shard_bags[k], x, w.mode, out=out, stream=s, after=rec)
             if w.train:
@@ -627,8 +662,20 @@ def run_ours(args, w):
                                              "frac": round(bw / peak, 4)}
         roof["touched_rows"] = int(statistics.mean(t["touched_rows"] for t in tbs))
 
+    if args.tier > 0:
+        link = host_link(torch, dev, 256 << 20, 256 << 20)
+        st = phases["stage"]
+        miss_bytes = statistics.mean(b.tier_misses for b in batches) * w.D * w.elem_bytes
+        roof["tier"] = {"cached_fraction": args.tier, "cache_rows": int(sum(tier.C)),
+                        "miss_lookups_per_step": int(statistics.mean(b.tier_misses for b in batches)),
+                        "lookups_per_step": int(statistics.mean(b.nnz for b in batches)),
+                        "host_bytes_per_step": int(miss_bytes),
+                        "stage_host_gbs": round(miss_bytes / (st["ms"] / 1e3) / 1e9, 1),
+                        "host_link_h2d_gbs": link["h2d_gbs"],
+                        "stage_frac_of_host_link": round(miss_bytes / (st["ms"] / 1e3) / 1e9 / link["h2d_gbs"], 4)}
+
     e2e = None
-    if not args.no_e2e and args.shards == 1 and not args.hash and args.op == "fused":
+    if not args.no_e2e and args.shards == 1 and not args.hash and args.op == "fused" and args.tier == 0:
         e2e = (run_e2e_train(args, w, tables, batches, dev, dl, torch, world, side) if w.train
                else run_e2e(args, w, tables, batches, dev, dl, torch, world))
         e2e["host_link"] = host_link(torch, dev, e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
@@ -659,7 +706,7 @@ def passes_for_rows(total_rows: int) -> int:
 
 def launches_per_step(args, w, plan=None) -> int:
     """Kernels of this library one step launches."""
-    n = 1 if args.hash else 0
+    n = (1 if args.hash else 0) + (1 if args.tier > 0 else 0)
     if plan is not None:
         G = plan.G
         n += G + 1 + plan.H  # lookup per table shard, exchange, interaction per sample shard
@@ -685,6 +732,7 @@ def kernel_of_phase(args, w, phase) -> str:
             "backward": "dlrm_sparse_bwd_update kernels (interaction backward, keys, radix sort, row updates; "
                         f"{args.rule})",
             "hash": "hash_kernel (raw ID mod V_t)",
+            "stage": "stage_kernel (cache slots, misses copied from host memory)",
             "lookup": "embbag_kernel (embedding-bag lookup, a lane group per bag"
                       + (", once per table shard)" if args.shards > 1 else ")"),
             "exchange": "exchange_kernel (all-to-all of the pooled vectors between logical shards)",
@@ -883,6 +931,9 @@ def main():
     if args.op == "embbag":
         w.name += " [embedding-bag lookup alone]"
         w.train = False  # a training workload's bags, looked up only
+    if args.tier > 0:
+        w.name += f" [tables in pinned host memory, device cache of {args.tier:g} of each table's rows]"
+        w.train = False  # the forward of a training workload's bags
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -25,6 +25,7 @@ DLRM_ERR_BAD_OFFSETS = 4
 DLRM_ERR_TIMEOUT = 8
 DLRM_ERR_CUDA = 16
 DLRM_ERR_UNSUPPORTED = 32
+DLRM_ERR_CAPACITY = 64
 MAX_TABLES = 128
 STATIC_SCRATCH_BYTES = 32 << 20  # DLRM_STATIC_SCRATCH_BYTES
 
@@ -35,7 +36,7 @@ _ITYPES = {torch.int32: 0, torch.int64: 1}
 C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sparse_fwd_host",
              "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_update",
              "dlrm_interact_bwd", "dlrm_embbag_bwd_workspace_size", "dlrm_embbag_bwd_update", "dlrm_hash_indices",
-             "dlrm_pooled_exchange",
+             "dlrm_pooled_exchange", "dlrm_tier_init", "dlrm_tier_cache_fill", "dlrm_tier_stage",
              "dlrm_sparse_bwd_adagrad_static", "dlrm_status_string", "dlrm_abi_version")
 _RULES = {"adagrad": 0, "sgd": 1}
 
@@ -48,6 +49,14 @@ class DlrmTables(ctypes.Structure):
 class DlrmBags(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("nnz", ctypes.c_int64), ("index_type", ctypes.c_int32),
                 ("indices", ctypes.c_void_p), ("offsets", ctypes.c_void_p)]
+
+
+class DlrmTieredTables(ctypes.Structure):
+    _fields_ = [("num_tables", ctypes.c_int32), ("dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("host_data", ctypes.POINTER(ctypes.c_void_p)), ("num_rows", ctypes.POINTER(ctypes.c_int64)),
+                ("slot_of", ctypes.POINTER(ctypes.c_void_p)), ("slot_row", ctypes.POINTER(ctypes.c_void_p)),
+                ("cache", ctypes.POINTER(ctypes.c_void_p)), ("cache_rows", ctypes.POINTER(ctypes.c_int64)),
+                ("stage_rows", ctypes.POINTER(ctypes.c_int64))]
 
 
 class DlrmUpdate(ctypes.Structure):
@@ -90,6 +99,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dlrm_embbag_bwd_update": ([T, B, i32, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P, P], i32),
         "dlrm_hash_indices": ([ctypes.POINTER(ctypes.c_int64), i32, i64, i64, P, P, i32, P, P, P], i32),
         "dlrm_pooled_exchange": ([P, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), i32, P], i32),
+        "dlrm_tier_init": ([ctypes.POINTER(DlrmTieredTables), P], i32),
+        "dlrm_tier_cache_fill": ([ctypes.POINTER(DlrmTieredTables), i32, P, i64, P, P], i32),
+        "dlrm_tier_stage": ([ctypes.POINTER(DlrmTieredTables), B, P, P, P, P], i32),
         "dlrm_sparse_bwd_adagrad_static": ([T, B, i32, P, P, P, P, ctypes.POINTER(ctypes.c_void_p),
                                             ctypes.c_float, ctypes.c_float, P, P], i32),
         "dlrm_status_string": ([i32], ctypes.c_char_p),
@@ -492,3 +504,98 @@ def dlrm_hash_indices(num_rows, raw_ids, offsets, rows=None, index_dtype=None, s
                                    status.data_ptr() if status is not None else None, _stream_ptr(stream, dev))
     _raise(st, "dlrm_hash_indices")
     return rows
+
+
+class TieredTables:
+    """Tables kept in pinned host memory with a device cache of hot rows (dlrm_tiered_tables).
+
+    host_tables: 2-D CPU tensors in pinned memory (tensor.pin_memory()), equal width and dtype; on a system
+    with unified addressing their addresses are readable by the device.  cache_rows / stage_rows: per table
+    (or one value for all) the device cache slots C_t and the staging rows M_t for a batch's misses.
+    Device memory: (C_t + M_t) rows, V_t int32 map entries and C_t int64 slot entries per table."""
+
+    def __init__(self, host_tables, cache_rows, stage_rows, device="cuda", stream=None):
+        host_tables = list(host_tables)
+        if not host_tables:
+            raise ValueError("need at least one table")
+        D, dt = host_tables[0].shape[1], host_tables[0].dtype
+        for i, t in enumerate(host_tables):
+            if t.is_cuda or not t.is_pinned() or not t.is_contiguous() or t.dim() != 2 or t.shape[1] != D or \
+                    t.dtype != dt:
+                raise ValueError(f"host table {i} must be a contiguous 2-D pinned CPU tensor of the common shape")
+        if dt not in _DTYPES:
+            raise ValueError(f"unsupported table dtype {dt}")
+        T = len(host_tables)
+        C = [int(cache_rows)] * T if isinstance(cache_rows, int) else [int(c) for c in cache_rows]
+        M = [int(stage_rows)] * T if isinstance(stage_rows, int) else [int(m) for m in stage_rows]
+        V = [t.shape[0] for t in host_tables]
+        self.host, self.T, self.D, self.dtype = host_tables, T, D, dt
+        self.C, self.M, self.V = C, M, V
+        self.device = torch.device(device)
+        self.slot_of = [torch.empty(v, dtype=torch.int32, device=self.device) for v in V]
+        self.slot_row = [torch.empty(max(c, 1), dtype=torch.int64, device=self.device) for c in C]
+        self.cache = [torch.empty((c + m, D), dtype=dt, device=self.device) for c, m in zip(C, M)]
+        self.counters = torch.empty(T, dtype=torch.int32, device=self.device)
+        self._arr = dict(
+            host=(ctypes.c_void_p * T)(*[t.data_ptr() for t in host_tables]),
+            rows=(ctypes.c_int64 * T)(*V),
+            slot_of=(ctypes.c_void_p * T)(*[x.data_ptr() for x in self.slot_of]),
+            slot_row=(ctypes.c_void_p * T)(*[x.data_ptr() for x in self.slot_row]),
+            cache=(ctypes.c_void_p * T)(*[x.data_ptr() if x.numel() else None for x in self.cache]),
+            C=(ctypes.c_int64 * T)(*C), M=(ctypes.c_int64 * T)(*M))
+        a = self._arr
+        self.c = DlrmTieredTables(T, D, _DTYPES[dt], a["host"], a["rows"], a["slot_of"], a["slot_row"], a["cache"],
+                                  a["C"], a["M"])
+        lib = load_library()
+        with torch.cuda.device(self.device):
+            _raise(lib.dlrm_tier_init(ctypes.byref(self.c), _stream_ptr(stream, self.device)), "dlrm_tier_init")
+        # the forward's view: table t = its device buffer of C_t + M_t rows
+        self.device_tables = Tables(self.cache)
+
+    def fill(self, table: int, rows, status=None, stream=None):
+        """Make `rows` (int64 device tensor of distinct row ids, at most C_t) the cache of `table`."""
+        lib = load_library()
+        _check_cuda(rows, "rows", torch.int64)
+        with torch.cuda.device(self.device):
+            st = lib.dlrm_tier_cache_fill(ctypes.byref(self.c), int(table), rows.data_ptr() if rows.numel() else None,
+                                          rows.numel(), status.data_ptr() if status is not None else None,
+                                          _stream_ptr(stream, self.device))
+        _raise(st, "dlrm_tier_cache_fill")
+
+    def stage(self, indices, offsets, out=None, status=None, stream=None):
+        """Rewrite a batch's indices into rows of the device buffers (misses copied in from host memory).
+        Returns the rewritten indices (dtype of `indices`), to pass with the same offsets and
+        self.device_tables to the forward entry points."""
+        lib = load_library()
+        B = _batch(offsets, self.T)
+        if out is None:
+            out = torch.empty_like(indices)
+        _check_cuda(out, "out", indices.dtype)
+        bags = _bags(indices, offsets, B)
+        dev = _device(indices, offsets, out, status, self.counters)
+        with torch.cuda.device(dev):
+            st = lib.dlrm_tier_stage(ctypes.byref(self.c), ctypes.byref(bags), out.data_ptr() if out.numel() else None,
+                                     self.counters.data_ptr(), status.data_ptr() if status is not None else None,
+                                     _stream_ptr(stream, dev))
+        _raise(st, "dlrm_tier_stage")
+        return out
+
+
+def hot_rows(indices, offsets, B: int, T: int, capacity, num_rows=None):
+    """Host-side cache policy: per table, the `capacity` rows looked up most often in the given batches
+    (numpy arrays of one batch, or lists of them), ties broken by the lower row id.  Returns a list of
+    int64 numpy arrays."""
+    import numpy as np
+    idx_list = indices if isinstance(indices, (list, tuple)) else [indices]
+    off_list = offsets if isinstance(offsets, (list, tuple)) else [offsets]
+    caps = [capacity] * T if isinstance(capacity, int) else list(capacity)
+    out = []
+    for t in range(T):
+        seg = np.concatenate([np.asarray(i)[np.asarray(o)[t * B]:np.asarray(o)[(t + 1) * B]]
+                              for i, o in zip(idx_list, off_list)]).astype(np.int64)
+        if num_rows is not None:
+            seg = seg[(seg >= 0) & (seg < num_rows[t])]
+        rows, counts = np.unique(seg, return_counts=True)
+        order = np.lexsort((rows, -counts))
+        out.append(rows[order][:caps[t]])
+    return out

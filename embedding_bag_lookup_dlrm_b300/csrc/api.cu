@@ -81,6 +81,7 @@ const char* dlrm_status_string(dlrm_status s)
     if (s & DLRM_ERR_TIMEOUT) return "device wait timed out";
     if (s & DLRM_ERR_CUDA) return "CUDA error";
     if (s & DLRM_ERR_UNSUPPORTED) return "unsupported configuration";
+    if (s & DLRM_ERR_CAPACITY) return "staging capacity exceeded";
     return "unknown status";
 }
 
@@ -373,6 +374,89 @@ dlrm_status dlrm_pooled_exchange(const dlrm_shard_plan* plan, float* const* by_t
     a.D = D;
     a.to_sample = to_sample;
     return dlrm::launch_exchange(a, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+dlrm_status check_tiered(const dlrm_tiered_tables* t)
+{
+    if (t == nullptr || t->host_data == nullptr || t->num_rows == nullptr || t->slot_of == nullptr ||
+        t->slot_row == nullptr || t->cache == nullptr || t->cache_rows == nullptr || t->stage_rows == nullptr)
+        return DLRM_ERR_INVALID_ARG;
+    if (t->num_tables < 1 || t->num_tables > DLRM_MAX_TABLES) return DLRM_ERR_INVALID_ARG;
+    if (t->dtype != DLRM_F32 && t->dtype != DLRM_BF16) return DLRM_ERR_INVALID_ARG;
+    if (t->dim <= 0 || t->dim > 256 || t->dim % 4 != 0) return DLRM_ERR_INVALID_ARG;
+    if (!dim_supported(t->dim)) return DLRM_ERR_UNSUPPORTED;
+    for (int i = 0; i < t->num_tables; ++i) {
+        if (t->num_rows[i] < 1 || t->cache_rows[i] < 0 || t->stage_rows[i] < 0) return DLRM_ERR_INVALID_ARG;
+        if (t->cache_rows[i] + t->stage_rows[i] > INT32_MAX) return DLRM_ERR_UNSUPPORTED;  // 32-bit slots
+        if (t->host_data[i] == nullptr || !aligned16(t->host_data[i]) || t->slot_of[i] == nullptr) return DLRM_ERR_INVALID_ARG;
+        if (t->cache_rows[i] + t->stage_rows[i] > 0 && (t->cache[i] == nullptr || !aligned16(t->cache[i])))
+            return DLRM_ERR_INVALID_ARG;
+        if (t->cache_rows[i] > 0 && t->slot_row[i] == nullptr) return DLRM_ERR_INVALID_ARG;
+    }
+    return DLRM_OK;
+}
+
+int row_bytes_of(const dlrm_tiered_tables* t) { return t->dim * (t->dtype == DLRM_F32 ? 4 : 2); }
+
+}  // namespace
+
+extern "C" {
+
+dlrm_status dlrm_tier_init(const dlrm_tiered_tables* tables, cudaStream_t stream)
+{
+    dlrm_status st = check_tiered(tables);
+    if (st != DLRM_OK) return st;
+    for (int t = 0; t < tables->num_tables; ++t) {
+        st = dlrm::launch_tier_init(tables->slot_of[t], tables->num_rows[t], tables->slot_row[t],
+                                    tables->cache_rows[t], stream);
+        if (st != DLRM_OK) return st;
+    }
+    return DLRM_OK;
+}
+
+dlrm_status dlrm_tier_cache_fill(const dlrm_tiered_tables* tables, int32_t table, const int64_t* rows, int64_t n,
+                                 int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tiered(tables);
+    if (st != DLRM_OK) return st;
+    if (table < 0 || table >= tables->num_tables || n < 0 || n > tables->cache_rows[table] ||
+        (n > 0 && rows == nullptr))
+        return DLRM_ERR_INVALID_ARG;
+    return dlrm::launch_tier_fill(tables->host_data[table], tables->cache[table], tables->slot_of[table],
+                                  tables->slot_row[table], rows, n, tables->cache_rows[table], tables->num_rows[table],
+                                  row_bytes_of(tables), status_dev, stream);
+}
+
+dlrm_status dlrm_tier_stage(const dlrm_tiered_tables* tables, const dlrm_bags* bags, void* indices_out,
+                            int32_t* counters, int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tiered(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (counters == nullptr || (bags->nnz > 0 && indices_out == nullptr)) return DLRM_ERR_INVALID_ARG;
+    dlrm::TierArgs a;
+    memset(&a, 0, sizeof a);
+    for (int t = 0; t < tables->num_tables; ++t) {
+        a.host[t] = tables->host_data[t];
+        a.cache[t] = tables->cache[t];
+        a.slot_of[t] = tables->slot_of[t];
+        a.num_rows[t] = tables->num_rows[t];
+        a.cache_rows[t] = tables->cache_rows[t];
+        a.stage_rows[t] = tables->stage_rows[t];
+    }
+    a.indices = bags->indices;
+    a.offsets = bags->offsets;
+    a.counters = counters;
+    a.status = status_dev;
+    a.B = bags->batch;
+    a.nnz = bags->nnz;
+    a.T = tables->num_tables;
+    a.row_bytes = row_bytes_of(tables);
+    return dlrm::launch_tier_stage(a, bags->index_type, indices_out, stream);
 }
 
 dlrm_status dlrm_hash_indices(const int64_t* num_rows, int32_t num_tables, int64_t batch, int64_t nnz,

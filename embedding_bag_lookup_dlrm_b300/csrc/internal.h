@@ -123,4 +123,26 @@ struct ExchangeArgs {
 };
 dlrm_status launch_exchange(const ExchangeArgs& args, cudaStream_t stream);
 
+// Tables in host memory with a device cache: the staging of a batch's lookups.
+struct TierArgs {
+    const void* host[DLRM_MAX_TABLES];  // device-readable addresses of the host tables
+    void* cache[DLRM_MAX_TABLES];       // device: (C_t + M_t) rows
+    const int32_t* slot_of[DLRM_MAX_TABLES];
+    int64_t num_rows[DLRM_MAX_TABLES];
+    int64_t cache_rows[DLRM_MAX_TABLES];
+    int64_t stage_rows[DLRM_MAX_TABLES];
+    const void* indices;
+    const void* offsets;
+    int32_t* counters;  // T staging counters (zeroed by the launch)
+    int32_t* status;
+    int64_t B;
+    int64_t nnz;
+    int32_t T;
+    int32_t row_bytes;
+};
+dlrm_status launch_tier_stage(const TierArgs& args, int index_type, void* out, cudaStream_t stream);
+dlrm_status launch_tier_fill(const void* host, void* cache, int32_t* slot_of, int64_t* slot_row, const int64_t* rows,
+                             int64_t n, int64_t C, int64_t V, int row_bytes, int32_t* status, cudaStream_t stream);
+dlrm_status launch_tier_init(int32_t* slot_of, int64_t V, int64_t* slot_row, int64_t C, cudaStream_t stream);
+
 }  // namespace dlrm

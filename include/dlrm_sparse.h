@@ -66,7 +66,8 @@ enum {
     DLRM_ERR_BAD_OFFSETS = 4,  /* device: malformed CSR offsets */
     DLRM_ERR_TIMEOUT = 8,      /* device: a bounded wait gave up (work of that sample skipped) */
     DLRM_ERR_CUDA = 16,        /* a CUDA launch or copy returned an error */
-    DLRM_ERR_UNSUPPORTED = 32  /* valid request the library does not implement */
+    DLRM_ERR_UNSUPPORTED = 32, /* valid request the library does not implement */
+    DLRM_ERR_CAPACITY = 64     /* device: a staging area ran out of rows (those lookups pool as zero) */
 };
 
 typedef enum { DLRM_POOL_SUM = 0, DLRM_POOL_MEAN = 1 } dlrm_pool_mode;
@@ -306,6 +307,59 @@ typedef struct {
 dlrm_status dlrm_pooled_exchange(const dlrm_shard_plan *plan, float *const *by_table,
                                  float *const *by_sample, int32_t to_sample,
                                  cudaStream_t stream);
+
+/* ---- tables larger than device memory ------------------------------------
+ * "DLRM explained", "How do you size compute for a DLRM...": tables beyond
+ * device memory live in host RAM; "DLRM", robocikowo.com, CPU-inference
+ * paragraph.  Item popularity follows a power law, so a device cache of the
+ * hot rows takes most lookups.  Table t keeps its V_t rows in host memory the
+ * device can read (pinned and mapped: cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped; on systems with unified addressing every pinned
+ * allocation is), and in device memory a buffer of C_t + M_t rows: C_t cache
+ * slots, then M_t staging rows for a batch's misses; plus the map slot_of (the
+ * cache slot of each row, or -1) and its inverse slot_row (the row in each
+ * slot, or -1).  Forward only: a training step updates rows in device memory. */
+typedef struct {
+    int32_t num_tables;           /* T in [1, DLRM_MAX_TABLES] */
+    int32_t dim;                  /* D, as for dlrm_tables */
+    int32_t dtype;                /* dlrm_dtype */
+    const void *const *host_data; /* [T]: device-readable address of table t in host memory, V_t x D */
+    const int64_t *num_rows;      /* [T]: V_t >= 1 */
+    int32_t *const *slot_of;      /* [T]: device, V_t int32 */
+    int64_t *const *slot_row;     /* [T]: device, C_t int64 */
+    void *const *cache;           /* [T]: device, (C_t + M_t) x D elements, 16-byte aligned */
+    const int64_t *cache_rows;    /* [T]: C_t >= 0, < 2^31 */
+    const int64_t *stage_rows;    /* [T]: M_t >= 0, C_t + M_t < 2^31 */
+} dlrm_tiered_tables;               /* every array above is a HOST array */
+
+/* Empty every cache: slot_of = -1 and slot_row = -1 for every table.  Call
+ * once after allocating the maps, before any other tier call. */
+dlrm_status dlrm_tier_init(const dlrm_tiered_tables *tables, cudaStream_t stream);
+
+/* Make `rows` (device, n distinct row ids of table `table`, n <= C_t) the
+ * cache of that table: the rows leaving it get slot -1, rows[i] is copied from
+ * host memory into slot i, slots past n hold nothing.  A row id outside
+ * [0, V_t) sets DLRM_ERR_INDEX_OOB and leaves its slot empty.  Ordered on
+ * `stream` like every call: no batch staged before it sees the new cache, every
+ * batch staged after it does. */
+dlrm_status dlrm_tier_cache_fill(const dlrm_tiered_tables *tables, int32_t table,
+                                 const int64_t *rows, int64_t n, int32_t *status_dev,
+                                 cudaStream_t stream);
+
+/* Stage one batch: indices_out[p] (device, nnz entries of bags->index_type)
+ * becomes the row of lookup p in the device buffer of its table: its cache
+ * slot when cached, else the next staging row, into which the row is copied
+ * from host memory (duplicate misses get a row each); an index outside
+ * [0, V_t) becomes -1.  counters: device, T int32 of scratch (zeroed by the
+ * call).  When a table's M_t staging rows run out, DLRM_ERR_CAPACITY is set in
+ * *status_dev and the remaining misses become -1.  The forward entry points
+ * then run on tables {cache[t], C_t + M_t rows} with these indices and the same
+ * offsets, and give the result of the untiered tables bit for bit.  The
+ * staging rows belong to this batch until the forward that reads them has run
+ * on the stream. */
+dlrm_status dlrm_tier_stage(const dlrm_tiered_tables *tables, const dlrm_bags *bags,
+                            void *indices_out, int32_t *counters, int32_t *status_dev,
+                            cudaStream_t stream);
 
 /* Bytes of the fixed scratch behind dlrm_sparse_bwd_adagrad_static. */
 #define DLRM_STATIC_SCRATCH_BYTES (32u << 20)
