@@ -17,8 +17,9 @@
 // bit for bit: every lookup reads a bit-exact copy of its row.
 //
 // A warp takes 32 consecutive lookups (one lane each for the index, the table
-// search and the map), then copies the missed rows one by one, all 32 lanes on
-// a row (host reads over the link, 16 bytes a lane).
+// search and the map), then copies the missed rows four at a time, all 32
+// lanes on each row (host reads over the link, 16 bytes a lane, the four rows'
+// reads in flight together).
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,6 +27,7 @@ namespace dlrm {
 namespace {
 
 constexpr int kTierThreads = 256;
+constexpr int kMissRows = 4;  // missed rows a warp reads from host memory at once
 
 template <typename TI>
 __global__ void __launch_bounds__(kTierThreads) stage_kernel(const __grid_constant__ TierArgs a, TI* out)
@@ -75,17 +77,34 @@ __global__ void __launch_bounds__(kTierThreads) stage_kernel(const __grid_consta
             }
             out[p] = static_cast<TI>(dst);
         }
-        // the warp copies its missed rows, each by all lanes
+        // the warp copies its missed rows, each by all lanes, kMissRows rows' loads in flight before the stores
         uint32_t miss = __ballot_sync(0xffffffffu, src_row >= 0);
         while (miss != 0) {
-            const int l = __ffs(miss) - 1;
-            miss &= miss - 1;
-            const int tl = __shfl_sync(0xffffffffu, t, l);
-            const int64_t r = __shfl_sync(0xffffffffu, src_row, l);
-            const int64_t d = __shfl_sync(0xffffffffu, dst, l);
-            const uint4* s = reinterpret_cast<const uint4*>(static_cast<const char*>(a.host[tl]) + r * a.row_bytes);
-            uint4* q = reinterpret_cast<uint4*>(static_cast<char*>(a.cache[tl]) + d * a.row_bytes);
-            for (int c = lane; c < chunks; c += kWarp) q[c] = s[c];
+            const uint4* s[kMissRows];
+            uint4* q[kMissRows];
+#pragma unroll
+            for (int u = 0; u < kMissRows; ++u) {
+                s[u] = nullptr;
+                q[u] = nullptr;
+                if (miss != 0) {
+                    const int l = __ffs(miss) - 1;
+                    miss &= miss - 1;
+                    const int tl = __shfl_sync(0xffffffffu, t, l);
+                    const int64_t r = __shfl_sync(0xffffffffu, src_row, l);
+                    const int64_t d = __shfl_sync(0xffffffffu, dst, l);
+                    s[u] = reinterpret_cast<const uint4*>(static_cast<const char*>(a.host[tl]) + r * a.row_bytes);
+                    q[u] = reinterpret_cast<uint4*>(static_cast<char*>(a.cache[tl]) + d * a.row_bytes);
+                }
+            }
+            for (int c = lane; c < chunks; c += kWarp) {
+                uint4 v[kMissRows];
+#pragma unroll
+                for (int u = 0; u < kMissRows; ++u)
+                    if (s[u] != nullptr) v[u] = s[u][c];
+#pragma unroll
+                for (int u = 0; u < kMissRows; ++u)
+                    if (q[u] != nullptr) q[u][c] = v[u];
+            }
         }
     }
 }
