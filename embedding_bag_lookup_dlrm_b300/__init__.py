@@ -37,6 +37,8 @@ C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sp
              "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_update",
              "dlrm_interact_bwd", "dlrm_embbag_bwd_workspace_size", "dlrm_embbag_bwd_update", "dlrm_hash_indices",
              "dlrm_pooled_exchange", "dlrm_tier_init", "dlrm_tier_cache_fill", "dlrm_tier_stage",
+             "dlrm_fc_fwd", "dlrm_fc_bwd_workspace_size", "dlrm_fc_bwd_sgd", "dlrm_head_bce_workspace_size",
+             "dlrm_head_bce_sgd",
              "dlrm_sparse_bwd_adagrad_static", "dlrm_status_string", "dlrm_abi_version")
 _RULES = {"adagrad": 0, "sgd": 1}
 
@@ -99,6 +101,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dlrm_embbag_bwd_update": ([T, B, i32, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P, P], i32),
         "dlrm_hash_indices": ([ctypes.POINTER(ctypes.c_int64), i32, i64, i64, P, P, i32, P, P, P], i32),
         "dlrm_pooled_exchange": ([P, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), i32, P], i32),
+        "dlrm_fc_fwd": ([P, P, P, i64, i32, i32, i32, P, P, P], i32),
+        "dlrm_fc_bwd_workspace_size": ([i64, i32, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
+        "dlrm_fc_bwd_sgd": ([P, P, P, P, P, i64, i32, i32, i32, ctypes.c_float, P, P, ctypes.c_size_t, P, P], i32),
+        "dlrm_head_bce_workspace_size": ([i64, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
+        "dlrm_head_bce_sgd": ([P, P, P, P, i64, i32, ctypes.c_float, P, P, P, P, ctypes.c_size_t, P], i32),
         "dlrm_tier_init": ([ctypes.POINTER(DlrmTieredTables), P], i32),
         "dlrm_tier_cache_fill": ([ctypes.POINTER(DlrmTieredTables), i32, P, i64, P, P], i32),
         "dlrm_tier_stage": ([ctypes.POINTER(DlrmTieredTables), B, P, P, P, P], i32),
@@ -599,3 +606,179 @@ def hot_rows(indices, offsets, B: int, T: int, capacity, num_rows=None):
         order = np.lexsort((rows, -counts))
         out.append(rows[order][:caps[t]])
     return out
+
+
+# ---------------------------------------------------------------------------
+# the dense layers around the sparse path
+# ---------------------------------------------------------------------------
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def dlrm_fc_fwd(x, w, b=None, relu=True, y=None, status=None, stream=None):
+    """y = act(x W^T + b) on the tensor cores; x [M, in], w [out, in], b [out] or None."""
+    lib = load_library()
+    for name, t in (("x", x), ("w", w)):
+        _check_cuda(t, name, torch.float32)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("w must be [out_dim, in_dim]")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    dev = _device(x, w, b, y, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_fc_fwd(x.data_ptr(), w.data_ptr(), _ptr(b), M, K, N, 1 if relu else 0, y.data_ptr(),
+                             _ptr(status), _stream_ptr(stream, dev))
+    _raise(st, "dlrm_fc_fwd")
+    return y
+
+
+def dlrm_fc_bwd_sgd(x, w, b, y, dy, lr, relu=True, dx=None, want_dx=True, workspace=None, status=None, stream=None):
+    """The layer's backward with plain SGD on w (and b): returns dx [M, in] (None when not wanted)."""
+    lib = load_library()
+    M, K = x.shape
+    N = w.shape[0]
+    if want_dx and dx is None:
+        dx = torch.empty((M, K), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _raise(lib.dlrm_fc_bwd_workspace_size(M, K, N, ctypes.byref(n)), "dlrm_fc_bwd_workspace_size")
+        workspace = torch.empty(max(n.value, 16), dtype=torch.uint8, device=x.device)
+    dev = _device(x, w, b, y, dy, dx, workspace, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_fc_bwd_sgd(x.data_ptr(), w.data_ptr(), _ptr(b), _ptr(y), dy.data_ptr(), M, K, N,
+                                 1 if relu else 0, float(lr), _ptr(dx) if want_dx else None, workspace.data_ptr(),
+                                 workspace.numel(), _ptr(status), _stream_ptr(stream, dev))
+    _raise(st, "dlrm_fc_bwd_sgd")
+    return dx if want_dx else None
+
+
+def fc_bwd_workspace_size(M, K, N) -> int:
+    n = ctypes.c_size_t(0)
+    _raise(load_library().dlrm_fc_bwd_workspace_size(M, K, N, ctypes.byref(n)), "dlrm_fc_bwd_workspace_size")
+    return int(n.value)
+
+
+def dlrm_head_bce_sgd(h, w, b, label, lr, prob=None, loss=None, dh=None, workspace=None, stream=None):
+    """Logit, sigmoid, mean BCE, its gradient dh, and SGD on w [in] and b [1]; returns (prob, loss, dh)."""
+    lib = load_library()
+    M, K = h.shape
+    if prob is None:
+        prob = torch.empty(M, dtype=torch.float32, device=h.device)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=h.device)
+    if dh is None:
+        dh = torch.empty((M, K), dtype=torch.float32, device=h.device)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _raise(lib.dlrm_head_bce_workspace_size(M, K, ctypes.byref(n)), "dlrm_head_bce_workspace_size")
+        workspace = torch.empty(max(n.value, 16), dtype=torch.uint8, device=h.device)
+    dev = _device(h, w, b, label, prob, loss, dh, workspace)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_head_bce_sgd(h.data_ptr(), w.data_ptr(), b.data_ptr(), label.data_ptr(), M, K, float(lr),
+                                   prob.data_ptr(), loss.data_ptr(), dh.data_ptr(), workspace.data_ptr(),
+                                   workspace.numel(), _stream_ptr(stream, dev))
+    _raise(st, "dlrm_head_bce_sgd")
+    return prob, loss, dh
+
+
+class DLRMModel:
+    """A whole DLRM around the sparse path, every step in the C library: the bottom MLP (FC + ReLU layers
+    ending at width D), the fused sparse forward, the top MLP (FC + ReLU layers) and a 1-wide sigmoid head
+    with the mean BCE loss; the backward with plain SGD on the MLP weights and row-wise Adagrad (or SGD) on
+    the embedding rows.
+
+    bottom: [(W, b), ...] fp32 CUDA tensors, W [out, in], the last out = D; top: the same, the first
+    in = D + N(N-1)/2; head: (w [in], b [1])."""
+
+    def __init__(self, tables, bottom, top, head):
+        self.tables = _tables(tables)
+        self.bottom, self.top, self.head = bottom, top, head
+        self._buf = {}
+
+    def _get(self, key, shape, dtype=torch.float32):
+        t = self._buf.get(key)
+        dev = self.head[0].device
+        if t is None or tuple(t.shape) != tuple(shape):
+            t = torch.empty(shape, dtype=dtype, device=dev)
+            self._buf[key] = t
+        return t
+
+    def _ws(self, key, nbytes):
+        t = self._buf.get(key)
+        if t is None or t.numel() < nbytes:
+            t = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.head[0].device)
+            self._buf[key] = t
+        return t
+
+    def forward(self, dense_in, indices, offsets, mode="sum", stream=None, after=None):
+        """Bottom MLP, sparse forward (pooled vectors saved), top MLP; returns the top MLP's output."""
+        B = dense_in.shape[0]
+        h = dense_in
+        self.bot_in = [h]
+        for i, (w, b) in enumerate(self.bottom):
+            h = dlrm_fc_fwd(h, w, b, True, y=self._get(("bot", i), (B, w.shape[0])), stream=stream)
+            self.bot_in.append(h)
+        if after:
+            after("bottom_fwd")
+        x = h
+        N = self.tables.T + 1
+        out = self._get("out", (B, self.tables.D + N * (N - 1) // 2))
+        pooled = self._get("pooled", (B, self.tables.T, self.tables.D))
+        dlrm_sparse_fwd(self.tables, indices, offsets, x, mode, out=out, pooled_save=pooled, stream=stream)
+        if after:
+            after("sparse_fwd")
+        g = out
+        self.top_in = [g]
+        for i, (w, b) in enumerate(self.top):
+            g = dlrm_fc_fwd(g, w, b, True, y=self._get(("top", i), (B, w.shape[0])), stream=stream)
+            self.top_in.append(g)
+        if after:
+            after("top_fwd")
+        return g
+
+    def train_step(self, dense_in, indices, offsets, label, lr_mlp, lr_emb, eps=1e-8, accum=None, rule="adagrad",
+                   mode="sum", stream=None, side_stream=None, after=None):
+        """One training step; returns (loss [1], prob [B]) as device tensors."""
+        B = dense_in.shape[0]
+        g = self.forward(dense_in, indices, offsets, mode, stream, after)
+        w, b = self.head
+        prob, loss, dh = dlrm_head_bce_sgd(g, w, b, label, lr_mlp, prob=self._get("prob", (B,)),
+                                           loss=self._get("loss", (1,)), dh=self._get("dh", (B, w.shape[0])),
+                                           workspace=self._ws("ws_head", _head_ws(B, w.shape[0])), stream=stream)
+        if after:
+            after("head")
+        dy = dh
+        for i in range(len(self.top) - 1, -1, -1):
+            W, bb = self.top[i]
+            xin, yout = self.top_in[i], self.top_in[i + 1]
+            dy = dlrm_fc_bwd_sgd(xin, W, bb, yout, dy, lr_mlp, True, dx=self._get(("dtop", i), tuple(xin.shape)),
+                                 workspace=self._ws(("ws_top", i), fc_bwd_workspace_size(B, W.shape[1], W.shape[0])),
+                                 stream=stream)
+        if after:
+            after("top_bwd")
+        x = self.bot_in[-1]
+        gx = self._get("grad_x", (B, self.tables.D))
+        ws = self._ws("ws_sparse", dlrm_sparse_bwd_workspace_size(self.tables, indices, offsets))
+        dlrm_sparse_bwd_update(self.tables, indices, offsets, x, self._buf["pooled"], dy, rule, lr_emb, eps, accum,
+                               mode, grad_dense=gx, workspace=ws, stream=stream, side_stream=side_stream)
+        if after:
+            after("sparse_bwd")
+        dy = gx
+        for i in range(len(self.bottom) - 1, -1, -1):
+            W, bb = self.bottom[i]
+            xin, yout = self.bot_in[i], self.bot_in[i + 1]
+            dy = dlrm_fc_bwd_sgd(xin, W, bb, yout, dy, lr_mlp, True,
+                                 dx=self._get(("dbot", i), tuple(xin.shape)) if i > 0 else None, want_dx=i > 0,
+                                 workspace=self._ws(("ws_bot", i), fc_bwd_workspace_size(B, W.shape[1], W.shape[0])),
+                                 stream=stream)
+        if after:
+            after("bottom_bwd")
+        return loss, prob
+
+
+def _head_ws(M, K) -> int:
+    n = ctypes.c_size_t(0)
+    _raise(load_library().dlrm_head_bce_workspace_size(M, K, ctypes.byref(n)), "dlrm_head_bce_workspace_size")
+    return int(n.value)

@@ -459,6 +459,73 @@ dlrm_status dlrm_tier_stage(const dlrm_tiered_tables* tables, const dlrm_bags* b
     return dlrm::launch_tier_stage(a, bags->index_type, indices_out, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+bool fc_dims_ok(int64_t batch, int32_t in_dim, int32_t out_dim)
+{
+    return batch >= 1 && batch <= (int64_t{1} << 31) && in_dim >= 1 && in_dim <= 65536 && out_dim >= 1 &&
+           out_dim <= 65536;
+}
+
+}  // namespace
+
+extern "C" {
+
+dlrm_status dlrm_fc_fwd(const float* x, const float* w, const float* b, int64_t batch, int32_t in_dim,
+                        int32_t out_dim, int32_t act, float* y, int32_t* status_dev, cudaStream_t stream)
+{
+    if (x == nullptr || w == nullptr || y == nullptr || !fc_dims_ok(batch, in_dim, out_dim)) return DLRM_ERR_INVALID_ARG;
+    if (act != DLRM_ACT_NONE && act != DLRM_ACT_RELU) return DLRM_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (b != nullptr && !aligned16(b))) return DLRM_ERR_INVALID_ARG;
+    return dlrm::launch_fc_fwd(x, w, b, batch, in_dim, out_dim, act == DLRM_ACT_RELU, y, status_dev, stream);
+}
+
+dlrm_status dlrm_fc_bwd_workspace_size(int64_t batch, int32_t in_dim, int32_t out_dim, size_t* bytes)
+{
+    if (bytes == nullptr || !fc_dims_ok(batch, in_dim, out_dim)) return DLRM_ERR_INVALID_ARG;
+    *bytes = dlrm::fc_bwd_workspace_bytes(batch, in_dim, out_dim);
+    return DLRM_OK;
+}
+
+dlrm_status dlrm_fc_bwd_sgd(const float* x, float* w, float* b, const float* y, const float* dy, int64_t batch,
+                            int32_t in_dim, int32_t out_dim, int32_t act, float lr, float* dx, void* workspace,
+                            size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream)
+{
+    if (x == nullptr || w == nullptr || dy == nullptr || workspace == nullptr || !fc_dims_ok(batch, in_dim, out_dim))
+        return DLRM_ERR_INVALID_ARG;
+    if (act != DLRM_ACT_NONE && act != DLRM_ACT_RELU) return DLRM_ERR_INVALID_ARG;
+    if (act == DLRM_ACT_RELU && y == nullptr) return DLRM_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(workspace) || (y != nullptr && !aligned16(y)) ||
+        (dx != nullptr && !aligned16(dx)) || (b != nullptr && !aligned16(b)))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < dlrm::fc_bwd_workspace_bytes(batch, in_dim, out_dim)) return DLRM_ERR_INVALID_ARG;
+    return dlrm::launch_fc_bwd_sgd(x, w, b, y, dy, batch, in_dim, out_dim, act == DLRM_ACT_RELU, lr, dx, workspace,
+                                   status_dev, stream);
+}
+
+dlrm_status dlrm_head_bce_workspace_size(int64_t batch, int32_t in_dim, size_t* bytes)
+{
+    if (bytes == nullptr || batch < 1 || batch > (int64_t{1} << 31) || in_dim < 1) return DLRM_ERR_INVALID_ARG;
+    if (in_dim > 1024) return DLRM_ERR_UNSUPPORTED;
+    *bytes = dlrm::head_workspace_bytes(batch, in_dim);
+    return DLRM_OK;
+}
+
+dlrm_status dlrm_head_bce_sgd(const float* h, float* w, float* b, const float* label, int64_t batch, int32_t in_dim,
+                              float lr, float* prob, float* loss, float* dh, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream)
+{
+    if (h == nullptr || w == nullptr || b == nullptr || label == nullptr || dh == nullptr || workspace == nullptr)
+        return DLRM_ERR_INVALID_ARG;
+    size_t need = 0;
+    dlrm_status st = dlrm_head_bce_workspace_size(batch, in_dim, &need);
+    if (st != DLRM_OK) return st;
+    if (workspace_bytes < need || !aligned16(workspace)) return DLRM_ERR_INVALID_ARG;
+    return dlrm::launch_head(h, w, b, label, batch, in_dim, lr, prob, loss, dh, workspace, stream);
+}
+
 dlrm_status dlrm_hash_indices(const int64_t* num_rows, int32_t num_tables, int64_t batch, int64_t nnz,
                               const uint64_t* raw_ids, const void* offsets, int32_t index_type, void* rows,
                               int32_t* status_dev, cudaStream_t stream)

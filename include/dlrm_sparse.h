@@ -361,6 +361,51 @@ dlrm_status dlrm_tier_stage(const dlrm_tiered_tables *tables, const dlrm_bags *b
                             void *indices_out, int32_t *counters, int32_t *status_dev,
                             cudaStream_t stream);
 
+/* ---- the dense layers around the sparse path ------------------------------
+ * "DLRM", robocikowo.com, "Forward pass" step (1) (bottom MLP: FC layers
+ * with ReLU ending at width D), step (4) and the top-MLP paragraph (FC layers
+ * with ReLU, a sigmoid output), training with SGD; the hardware paragraph:
+ * the MLPs are ordinary GEMMs on the tensor cores.  fp32 in and out; the
+ * products run on the tcgen05 tensor cores with each fp32 operand split into
+ * two bf16 values (hi + lo; hi*hi + hi*lo + lo*hi accumulated in fp32), which
+ * keeps about 16 significant bits of every product (relative error below
+ * 2^-16 of sum |a_k b_k|).  All matrices row-major, device memory, 16-byte
+ * aligned; W is out_dim x in_dim (y = x W^T + b). */
+typedef enum { DLRM_ACT_NONE = 0, DLRM_ACT_RELU = 1 } dlrm_activation;
+
+/* y[batch][out_dim] = act(x[batch][in_dim] W^T + b); b may be NULL (no bias).
+ * in_dim, out_dim in [1, 65536], batch in [1, 2^31]. */
+dlrm_status dlrm_fc_fwd(const float *x, const float *w, const float *b, int64_t batch,
+                        int32_t in_dim, int32_t out_dim, int32_t act, float *y,
+                        int32_t *status_dev, cudaStream_t stream);
+
+/* Bytes of device workspace dlrm_fc_bwd_sgd needs. */
+dlrm_status dlrm_fc_bwd_workspace_size(int64_t batch, int32_t in_dim, int32_t out_dim, size_t *bytes);
+
+/* The backward of dlrm_fc_fwd from dy (the gradient of y) with plain SGD:
+ *   dz = dy * [y > 0] (act = RELU; y is the forward's output) or dy;
+ *   dx = dz W  (written when dx is not NULL, with W before its update);
+ *   W -= lr * dz^T x;  b -= lr * sum over the batch of dz  (when b is not NULL).
+ * The sums over the batch run in a fixed order: bitwise reproducible. */
+dlrm_status dlrm_fc_bwd_sgd(const float *x, float *w, float *b, const float *y, const float *dy,
+                            int64_t batch, int32_t in_dim, int32_t out_dim, int32_t act,
+                            float lr, float *dx, void *workspace, size_t workspace_bytes,
+                            int32_t *status_dev, cudaStream_t stream);
+
+/* Bytes of device workspace dlrm_head_bce_sgd needs (in_dim <= 1024). */
+dlrm_status dlrm_head_bce_workspace_size(int64_t batch, int32_t in_dim, size_t *bytes);
+
+/* The output layer and the loss, forward and backward with SGD: per sample
+ * z = h . w + b, p = sigmoid(z) (written to prob when not NULL), the mean
+ * binary cross-entropy over the batch max(z,0) - z*label + log(1+exp(-|z|))
+ * (written to *loss, a device float, when not NULL); dz = (p - label) / batch;
+ * dh = dz * w (written, with w before its update); w -= lr * sum dz h,
+ * b -= lr * sum dz (b: one device float).  h: batch x in_dim; label: batch
+ * values (0 or 1, any value in [0, 1] accepted). */
+dlrm_status dlrm_head_bce_sgd(const float *h, float *w, float *b, const float *label, int64_t batch,
+                              int32_t in_dim, float lr, float *prob, float *loss, float *dh,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Bytes of the fixed scratch behind dlrm_sparse_bwd_adagrad_static. */
 #define DLRM_STATIC_SCRATCH_BYTES (32u << 20)
 
