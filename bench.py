@@ -65,6 +65,9 @@ def parse():
                    help="F > 0: the tables live in pinned host memory with a device cache of the fraction F of each "
                         "table's rows (the hottest in separate history batches); each step stages its lookups, then "
                         "runs the forward on the device buffers")
+    p.add_argument("--model", action="store_true",
+                   help="the whole DLRM training step on the training workload: bottom MLP 13-512-256-D, the sparse "
+                        "path, top MLP (D+K)-512-256, a 256-1 sigmoid head with BCE; SGD on the MLPs")
     p.add_argument("--hash", action="store_true",
                    help="the bags arrive as raw 64-bit IDs: the hashing pre-pass (ID mod V_t) runs in each step")
     return p.parse_args()
@@ -907,6 +910,128 @@ def run_e2e(args, w, tables, batches, dev, dl, torch, world):
                    "overlap the kernel of the next); wall clock over the timed steps"}
 
 
+MODEL_BOTTOM = (13, 512, 256)   # dense features -> ... -> D (the workload's width closes the stack)
+MODEL_TOP = (512, 256)          # (D + K) -> ... ; then the 1-wide head
+
+
+def run_model(args, w):
+    """The whole DLRM training step (bench.py --model) on one GPU, timed phase by phase."""
+    import torch
+
+    import embedding_bag_lookup_dlrm_b300 as dl
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    dl.load_library()
+    tabs = []
+    for t, V in enumerate(w.num_rows):
+        x = torch.empty((V, w.D), dtype=torch.float32, device=dev)
+        gen.fill_table_device(x.data_ptr(), "f32", w.seed, t, 0, V, w.D, torch.cuda.current_stream().cuda_stream)
+        tabs.append(x)
+    batches = gen.make_batches(w, list(range(N_ROTATE)))
+    rng = np.random.default_rng(w.seed)
+    dev_b = []
+    for b in batches:
+        dense_in = rng.standard_normal((w.B, MODEL_BOTTOM[0])).astype(np.float32)
+        label = (rng.random(w.B) < 0.25).astype(np.float32)
+        dev_b.append(tuple(torch.from_numpy(a).to(dev) for a in (dense_in, label, b.indices, b.offsets)))
+
+    def layer(fin, fout):  # uniform(+-1/sqrt(fan_in)), seeded
+        bound = 1.0 / np.sqrt(fin)
+        return (torch.from_numpy(rng.uniform(-bound, bound, (fout, fin)).astype(np.float32)).to(dev),
+                torch.from_numpy(rng.uniform(-bound, bound, fout).astype(np.float32)).to(dev))
+
+    bot_sizes = list(MODEL_BOTTOM) + [w.D]
+    top_sizes = [w.out_width] + list(MODEL_TOP)
+    bottom = [layer(a, c) for a, c in zip(bot_sizes, bot_sizes[1:])]
+    top = [layer(a, c) for a, c in zip(top_sizes, top_sizes[1:])]
+    hw, hb = layer(top_sizes[-1], 1)
+    model = dl.DLRMModel(tabs, bottom, top, (hw.reshape(-1).contiguous(), hb))
+    accum = [torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    side = torch.cuda.Stream(device=dev, priority=-100)
+
+    def step(i, rec):
+        dense_in, label, idx, off = dev_b[i % N_ROTATE]
+        model.train_step(dense_in, idx, off, label, 0.01, w.lr, w.eps, accum, mode=w.mode, stream=s,
+                         side_stream=side, after=rec)
+
+    with torch.cuda.stream(s):
+        for i in range(args.warmup):
+            flush.zero_()
+            step(i, None)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    marks = [[] for _ in range(args.steps)]
+
+    def recorder(i):
+        def rec(name):
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(s)
+            marks[i].append((name, ev))
+        return rec
+
+    with ClockSampler(0) as clk, torch.cuda.stream(s):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(s)
+            step(args.warmup + i, recorder(i))
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(m[-1][1]) for a, m in zip(starts, marks)]
+    phase_ms = {}
+    for a, m in zip(starts, marks):
+        prev = a
+        for name, ev in m:
+            phase_ms.setdefault(name, []).append(prev.elapsed_time(ev))
+            prev = ev
+    B = w.B
+    mac = lambda sizes: sum(a * c for a, c in zip(sizes, sizes[1:]))
+    flops = {"bottom_fwd": 2 * B * mac(bot_sizes), "top_fwd": 2 * B * mac(top_sizes),
+             "top_bwd": 4 * B * mac(top_sizes), "bottom_bwd": 4 * B * mac(bot_sizes) - 2 * B * bot_sizes[0] * bot_sizes[1]}
+    import json as _json
+    peaks_d = _json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"bf16_tflops": 1800.0}
+    tpk = float(peaks_d.get("bf16_tflops", 1800.0))
+    hbm, src = peaks()
+    tb = [train_bytes(w, b) for b in batches]
+    phases = {}
+    for name, ms in phase_ms.items():
+        t = statistics.mean(ms)
+        d = {"ms": round(t, 4)}
+        if name in flops:
+            tf = flops[name] / (t / 1e3) / 1e12
+            d.update({"fp32_gemm_tflops": round(tf, 2), "tensor_tflops": round(3 * tf, 2),
+                      "tensor_frac": round(3 * tf / tpk, 4)})
+        elif name == "sparse_fwd":
+            by = statistics.mean(x["forward"] for x in tb)
+            d.update({"bytes": int(by), "gbs": round(by / (t / 1e3) / 1e9, 1), "frac": round(by / (t / 1e3) / 1e9 / hbm, 4)})
+        elif name == "sparse_bwd":
+            by = statistics.mean(x["backward"] for x in tb)
+            d.update({"bytes": int(by), "gbs": round(by / (t / 1e3) / 1e9, 1), "frac": round(by / (t / 1e3) / 1e9 / hbm, 4)})
+        phases[name] = d
+    dom = max(phases, key=lambda n: phases[n]["ms"])
+    ms_per_step = statistics.mean(step_ms)
+    mlp_flops = sum(flops.values())
+    mlp_ms = sum(phases[n]["ms"] for n in flops)
+    line = {"metric": "DLRM training-step samples/s (bottom MLP, sparse path, top MLP, BCE) at 1 GPU",
+            "value": round(B * args.steps / (sum(step_ms) / 1e3), 1), "unit": "samples/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator; dense features N(0,1), labels Bernoulli(0.25))",
+            "config": dict(config_of(w, args), model=f"bottom {bot_sizes}, top {top_sizes + [1]}, sigmoid + BCE, "
+                                                     "SGD lr 0.01 on the MLPs"),
+            "roofline": {"phase": dom, "phases": phases,
+                         "mlp": {"fp32_gemm_flops": int(mlp_flops), "ms": round(mlp_ms, 4),
+                                 "tensor_tflops": round(3 * mlp_flops / (mlp_ms / 1e3) / 1e12, 2),
+                                 "peak_bf16_tflops": tpk,
+                                 "tensor_frac": round(3 * mlp_flops / (mlp_ms / 1e3) / 1e12 / tpk, 4),
+                                 "note": "three bf16 products per fp32 product (split-bf16)"},
+                         "peak_source": f"{src} (hbm_gbs; bf16_tflops)"},
+            "gpu_launches": None, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.warmup < 3:
@@ -936,6 +1061,10 @@ def main():
         w.train = False  # the forward of a training workload's bags
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.model:
+        if not w.train:
+            raise SystemExit("--model runs on the training workload (--workload 5)")
+        run_model(args, w)
     else:
         run_ours(args, w)
 
