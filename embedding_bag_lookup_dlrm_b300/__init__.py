@@ -37,7 +37,8 @@ C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sp
              "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_update",
              "dlrm_interact_bwd", "dlrm_embbag_bwd_workspace_size", "dlrm_embbag_bwd_update", "dlrm_hash_indices",
              "dlrm_pooled_exchange", "dlrm_tier_init", "dlrm_tier_cache_fill", "dlrm_tier_stage",
-             "dlrm_fc_fwd", "dlrm_fc_bwd_workspace_size", "dlrm_fc_bwd_sgd", "dlrm_head_bce_workspace_size",
+             "dlrm_fc_fwd_workspace_size", "dlrm_fc_fwd", "dlrm_fc_bwd_workspace_size", "dlrm_fc_bwd_sgd",
+             "dlrm_head_bce_workspace_size",
              "dlrm_head_bce_sgd",
              "dlrm_sparse_bwd_adagrad_static", "dlrm_status_string", "dlrm_abi_version")
 _RULES = {"adagrad": 0, "sgd": 1}
@@ -101,7 +102,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dlrm_embbag_bwd_update": ([T, B, i32, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P, P], i32),
         "dlrm_hash_indices": ([ctypes.POINTER(ctypes.c_int64), i32, i64, i64, P, P, i32, P, P, P], i32),
         "dlrm_pooled_exchange": ([P, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), i32, P], i32),
-        "dlrm_fc_fwd": ([P, P, P, i64, i32, i32, i32, P, P, P], i32),
+        "dlrm_fc_fwd_workspace_size": ([i64, i32, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
+        "dlrm_fc_fwd": ([P, P, P, i64, i32, i32, i32, P, P, ctypes.c_size_t, P, P], i32),
         "dlrm_fc_bwd_workspace_size": ([i64, i32, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
         "dlrm_fc_bwd_sgd": ([P, P, P, P, P, i64, i32, i32, i32, ctypes.c_float, P, P, ctypes.c_size_t, P, P], i32),
         "dlrm_head_bce_workspace_size": ([i64, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
@@ -615,7 +617,13 @@ def _ptr(t):
     return t.data_ptr() if t is not None else None
 
 
-def dlrm_fc_fwd(x, w, b=None, relu=True, y=None, status=None, stream=None):
+def fc_fwd_workspace_size(M, K, N) -> int:
+    n = ctypes.c_size_t(0)
+    _raise(load_library().dlrm_fc_fwd_workspace_size(M, K, N, ctypes.byref(n)), "dlrm_fc_fwd_workspace_size")
+    return int(n.value)
+
+
+def dlrm_fc_fwd(x, w, b=None, relu=True, y=None, workspace=None, status=None, stream=None):
     """y = act(x W^T + b) on the tensor cores; x [M, in], w [out, in], b [out] or None."""
     lib = load_library()
     for name, t in (("x", x), ("w", w)):
@@ -626,10 +634,12 @@ def dlrm_fc_fwd(x, w, b=None, relu=True, y=None, status=None, stream=None):
         raise ValueError("w must be [out_dim, in_dim]")
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=x.device)
-    dev = _device(x, w, b, y, status)
+    if workspace is None:
+        workspace = torch.empty(max(fc_fwd_workspace_size(M, K, N), 16), dtype=torch.uint8, device=x.device)
+    dev = _device(x, w, b, y, workspace, status)
     with torch.cuda.device(dev):
         st = lib.dlrm_fc_fwd(x.data_ptr(), w.data_ptr(), _ptr(b), M, K, N, 1 if relu else 0, y.data_ptr(),
-                             _ptr(status), _stream_ptr(stream, dev))
+                             workspace.data_ptr(), workspace.numel(), _ptr(status), _stream_ptr(stream, dev))
     _raise(st, "dlrm_fc_fwd")
     return y
 
@@ -718,7 +728,9 @@ class DLRMModel:
         h = dense_in
         self.bot_in = [h]
         for i, (w, b) in enumerate(self.bottom):
-            h = dlrm_fc_fwd(h, w, b, True, y=self._get(("bot", i), (B, w.shape[0])), stream=stream)
+            h = dlrm_fc_fwd(h, w, b, True, y=self._get(("bot", i), (B, w.shape[0])),
+                            workspace=self._ws("ws_fwd", fc_fwd_workspace_size(B, w.shape[1], w.shape[0])),
+                            stream=stream)
             self.bot_in.append(h)
         if after:
             after("bottom_fwd")
@@ -732,7 +744,9 @@ class DLRMModel:
         g = out
         self.top_in = [g]
         for i, (w, b) in enumerate(self.top):
-            g = dlrm_fc_fwd(g, w, b, True, y=self._get(("top", i), (B, w.shape[0])), stream=stream)
+            g = dlrm_fc_fwd(g, w, b, True, y=self._get(("top", i), (B, w.shape[0])),
+                            workspace=self._ws("ws_fwd", fc_fwd_workspace_size(B, w.shape[1], w.shape[0])),
+                            stream=stream)
             self.top_in.append(g)
         if after:
             after("top_fwd")

@@ -465,7 +465,7 @@ namespace {
 
 bool fc_dims_ok(int64_t batch, int32_t in_dim, int32_t out_dim)
 {
-    return batch >= 1 && batch <= (int64_t{1} << 31) && in_dim >= 1 && in_dim <= 65536 && out_dim >= 1 &&
+    return batch >= 1 && batch < (int64_t{1} << 31) && in_dim >= 1 && in_dim <= 65536 && out_dim >= 1 &&
            out_dim <= 65536;
 }
 
@@ -473,13 +473,24 @@ bool fc_dims_ok(int64_t batch, int32_t in_dim, int32_t out_dim)
 
 extern "C" {
 
-dlrm_status dlrm_fc_fwd(const float* x, const float* w, const float* b, int64_t batch, int32_t in_dim,
-                        int32_t out_dim, int32_t act, float* y, int32_t* status_dev, cudaStream_t stream)
+dlrm_status dlrm_fc_fwd_workspace_size(int64_t batch, int32_t in_dim, int32_t out_dim, size_t* bytes)
 {
-    if (x == nullptr || w == nullptr || y == nullptr || !fc_dims_ok(batch, in_dim, out_dim)) return DLRM_ERR_INVALID_ARG;
+    if (bytes == nullptr || !fc_dims_ok(batch, in_dim, out_dim)) return DLRM_ERR_INVALID_ARG;
+    *bytes = dlrm::fc_fwd_workspace_bytes(batch, in_dim, out_dim);
+    return DLRM_OK;
+}
+
+dlrm_status dlrm_fc_fwd(const float* x, const float* w, const float* b, int64_t batch, int32_t in_dim,
+                        int32_t out_dim, int32_t act, float* y, void* workspace, size_t workspace_bytes,
+                        int32_t* status_dev, cudaStream_t stream)
+{
+    if (x == nullptr || w == nullptr || y == nullptr || workspace == nullptr || !fc_dims_ok(batch, in_dim, out_dim))
+        return DLRM_ERR_INVALID_ARG;
     if (act != DLRM_ACT_NONE && act != DLRM_ACT_RELU) return DLRM_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (b != nullptr && !aligned16(b))) return DLRM_ERR_INVALID_ARG;
-    return dlrm::launch_fc_fwd(x, w, b, batch, in_dim, out_dim, act == DLRM_ACT_RELU, y, status_dev, stream);
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(workspace) || (b != nullptr && !aligned16(b)))
+        return DLRM_ERR_INVALID_ARG;
+    if (workspace_bytes < dlrm::fc_fwd_workspace_bytes(batch, in_dim, out_dim)) return DLRM_ERR_INVALID_ARG;
+    return dlrm::launch_fc_fwd(x, w, b, batch, in_dim, out_dim, act == DLRM_ACT_RELU, y, workspace, status_dev, stream);
 }
 
 dlrm_status dlrm_fc_bwd_workspace_size(int64_t batch, int32_t in_dim, int32_t out_dim, size_t* bytes)

@@ -146,8 +146,9 @@ dlrm_status launch_tier_fill(const void* host, void* cache, int32_t* slot_of, in
 dlrm_status launch_tier_init(int32_t* slot_of, int64_t V, int64_t* slot_row, int64_t C, cudaStream_t stream);
 
 // Dense layers (mlp.cu): y = act(x W^T + b) on the tensor cores, its backward with SGD, the sigmoid head.
+size_t fc_fwd_workspace_bytes(int64_t M, int32_t K, int32_t N);
 dlrm_status launch_fc_fwd(const float* x, const float* w, const float* b, int64_t M, int32_t K, int32_t N, int relu,
-                          float* y, int32_t* status, cudaStream_t stream);
+                          float* y, void* workspace, int32_t* status, cudaStream_t stream);
 size_t fc_bwd_workspace_bytes(int64_t M, int32_t K, int32_t N);
 dlrm_status launch_fc_bwd_sgd(const float* x, float* w, float* b, const float* y, const float* dy, int64_t M, int32_t K,
                               int32_t N, int relu, float lr, float* dx, void* workspace, int32_t* status,

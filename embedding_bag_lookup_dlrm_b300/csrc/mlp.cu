@@ -7,16 +7,17 @@
 //
 // GEMM.  C[M x N] = A[M x K] * B[N x K]^T with both operands K-major in global
 // memory (a row of A or B holds its K values contiguously), on the tcgen05
-// tensor cores: a CTA of 256 threads owns a 128 x 128 tile of C, walks K in
-// slices of 64, double-buffered in shared memory.  The threads load a slice of
-// fp32 A and B rows (16-byte loads where the rows allow), split each value v
-// into bf16 hi = bf16(v) and lo = bf16(v - hi) and store both into K-major
-// 128-byte-swizzled operand buffers; one thread issues hi*hi^T + hi*lo^T +
-// lo*hi^T (3 x 4 MMAs of 128 x 128 x 16) into a 128-column fp32 accumulator in
-// TMEM and commits them to the slice's mbarrier, while the threads load the
-// next slice.  The dropped lo*lo term and the rounding of lo stay below 2^-16
+// tensor cores: a CTA of 256 threads owns a 128 x 64 tile of C, walks K in
+// slices of 64, double-buffered in shared memory (96 KB: two CTAs per SM).  The
+// threads load a slice of fp32 A and B rows into registers (16-byte loads where
+// the rows allow), split each value v into bf16 hi = bf16(v) and lo =
+// bf16(v - hi) and store both into K-major 128-byte-swizzled operand buffers;
+// one thread issues hi*hi^T + hi*lo^T + lo*hi^T (3 x 4 MMAs of 128 x 64 x 16)
+// into a 64-column fp32 accumulator in TMEM and commits them to the slice's
+// mbarrier; the next slice's loads are issued right after, so they travel while
+// the MMAs run.  The dropped lo*lo term and the rounding of lo stay below 2^-16
 // relative to sum |a_k b_k|.  Epilogue: warp w reads TMEM lanes
-// 32 (w % 4) .. + 31 (rows of C), columns 64 (w / 4) .. + 63, adds the bias and
+// 32 (w % 4) .. + 31 (rows of C), columns 32 (w / 4) .. + 31, adds the bias and
 // applies ReLU, or writes a split-K partial.
 //
 // Backward of y = act(x W^T + b) from dy: dz = dy * [y > 0] (ReLU) or dy;
@@ -32,7 +33,12 @@
 // log(1 + exp(-|z|)) and dz = (p - y) / M, writes dh = dz w, and the block adds
 // its samples' dz h, dz and loss terms in a fixed order; a reduce kernel sums the
 // blocks' partials in order, writes the mean loss and applies SGD to w and b.
+#include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <string.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -41,97 +47,43 @@
 namespace dlrm {
 namespace {
 
-constexpr int kGThreads = 256;
+constexpr int kGThreads = 128;  // warp 0: TMA producer, warp 1: MMA issuer; all four: epilogue
 constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kSlice = kBM * kBK * 2;  // one bf16 operand slice, 16 KB (kBM == kBN)
-constexpr int kStage = 4 * kSlice;     // A hi, A lo, B hi, B lo
-constexpr int kGemmSmem = 2 * kStage + 1024 + 64;
+constexpr int kStages = 3;
+constexpr int kTile = kBM * kBK * 2;        // one bf16 operand tile, 16 KB (kBM == kBN)
+constexpr int kStage = 4 * kTile;           // A hi, A lo, B hi, B lo: 64 KB
+constexpr int kGemmSmem = kStages * kStage + 1024 + 128;
 constexpr uint32_t kFull = 0xffffffffu;
 
 struct GemmArgs {
-    const float* a;
-    const float* amask;  // optional: A multiplied by [amask > 0] (same layout, leading dimension lda)
-    const float* b;
-    const float* bias;   // optional, N values
+    CUtensorMap a_hi, a_lo, b_hi, b_lo;  // bf16 [rows x Kp], box 64 x 128, 128-byte swizzle
+    const float* bias;                   // optional, N values
     float* c;
-    int64_t lda, ldb, ldc;
+    int64_t ldc;
     int64_t M, N, K;
     int64_t k_per_split;   // reduction range of split z: [z * k_per_split, min(K, (z + 1) * k_per_split))
     int64_t split_stride;  // elements between the C partials of consecutive splits
     int relu;
-    int vec_a, vec_b;      // 16-byte loads allowed
     int32_t* status;
 };
 
-// Byte offset of (row, byte b of its 128-byte K extent) in a K-major 128-byte-swizzle operand slice.
-__device__ __forceinline__ uint32_t sw128(int row, int b)
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
 {
-    return row * 128 + ((((b >> 4) ^ (row & 7)) << 4) | (b & 15));
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 h)
-{
-    return static_cast<uint32_t>(__bfloat16_as_ushort(h.x)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h.y)) << 16);
-}
-
-__device__ __forceinline__ void split_store(unsigned char* hi, unsigned char* lo, int row, int kc, float4 v)
-{
-    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
-    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
-    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-    const uint32_t off = sw128(row, kc * 8);
-    *reinterpret_cast<uint2*>(hi + off) = make_uint2(bf16x2_bits(h01), bf16x2_bits(h23));
-    *reinterpret_cast<uint2*>(lo + off) = make_uint2(bf16x2_bits(l01), bf16x2_bits(l23));
-}
-
-// Rows r0 .. r0 + 127 (below R) and K values k0 .. k0 + 63 (below kend) of a K-major fp32 matrix into the
-// hi / lo slices; 8 float4 per thread, every load issued before the splits.
-__device__ __forceinline__ void load_slice(const float* src, const float* mask, int64_t ld, int vec, int64_t r0,
-                                           int64_t R, int64_t k0, int64_t kend, unsigned char* hi, unsigned char* lo)
-{
-    float4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = threadIdx.x + i * kGThreads;
-        const int row = idx >> 4, kc = idx & 15;
-        const int64_t r = r0 + row, k = k0 + kc * 4;
-        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < R) {
-            const float* p = src + r * ld + k;
-            if (vec && k + 3 < kend) {
-                v[i] = __ldg(reinterpret_cast<const float4*>(p));
-                if (mask != nullptr) {
-                    const float4 m = __ldg(reinterpret_cast<const float4*>(mask + r * ld + k));
-                    v[i] = make_float4(m.x > 0.f ? v[i].x : 0.f, m.y > 0.f ? v[i].y : 0.f, m.z > 0.f ? v[i].z : 0.f,
-                                       m.w > 0.f ? v[i].w : 0.f);
-                }
-            } else {
-                float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (k + j < kend) {
-                        e[j] = __ldg(p + j);
-                        if (mask != nullptr && !(__ldg(mask + r * ld + k + j) > 0.f)) e[j] = 0.f;
-                    }
-                v[i] = make_float4(e[0], e[1], e[2], e[3]);
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = threadIdx.x + i * kGThreads;
-        split_store(hi, lo, idx >> 4, idx & 15, v[i]);
-    }
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
 }
 
 __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs g)
 {
     extern __shared__ unsigned char gsm_raw[];
     unsigned char* sm = gsm_raw + ((1024u - (smem_addr(gsm_raw) & 1023u)) & 1023u);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * kStage);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + 2 * kStage + 16);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kStages * kStage);
+    uint64_t* empty = full + kStages;
+    uint64_t* done = empty + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kBM, n0 = static_cast<int64_t>(blockIdx.y) * kBN;
     const int64_t kb = static_cast<int64_t>(blockIdx.z) * g.k_per_split;
@@ -139,8 +91,11 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     const int nk = ke > kb ? static_cast<int>((ke - kb + kBK - 1) / kBK) : 0;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -151,60 +106,57 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    auto tile = [&](int s, int which) { return sm + s * kStage + which * kTile; };
 
-    auto stage_ptr = [&](int s, int which) { return sm + s * kStage + which * kSlice; };
     bool ok = true;
-    if (nk > 0) {
-        load_slice(g.a, g.amask, g.lda, g.vec_a, m0, g.M, kb, ke, stage_ptr(0, 0), stage_ptr(0, 1));
-        load_slice(g.b, nullptr, g.ldb, g.vec_b, n0, g.N, kb, ke, stage_ptr(0, 2), stage_ptr(0, 3));
-    }
-    for (int i = 0; i < nk; ++i) {
-        const int s = i & 1;
-        tc::fence_smem_for_mma();
-        __syncthreads();
-        if (threadIdx.x == 0) {
+    if (warp == 0 && lane == 0) {
+        // producer: stage s of slice i, once the MMAs of slice i - kStages have read it
+        for (int i = 0; i < nk && ok; ++i) {
+            const int s = i % kStages;
+            if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&full[s], kStage);
+            const int x = static_cast<int>(kb + static_cast<int64_t>(i) * kBK);
+            tma_load_2d(tile(s, 0), &g.a_hi, x, static_cast<int>(m0), &full[s]);
+            tma_load_2d(tile(s, 1), &g.a_lo, x, static_cast<int>(m0), &full[s]);
+            tma_load_2d(tile(s, 2), &g.b_hi, x, static_cast<int>(n0), &full[s]);
+            tma_load_2d(tile(s, 3), &g.b_lo, x, static_cast<int>(n0), &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: hi*hi, hi*lo, lo*hi over 4 steps of K = 16 per slice; each slice's stage released on commit
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+        for (int i = 0; i < nk && ok; ++i) {
+            const int s = i % kStages;
+            ok = mbar_wait_bounded(&full[s], (i / kStages) & 1);
+            if (!ok) break;
             tc::fence_after_sync();
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-            const uint32_t a_hi = smem_addr(stage_ptr(s, 0)), a_lo = smem_addr(stage_ptr(s, 1));
-            const uint32_t b_hi = smem_addr(stage_ptr(s, 2)), b_lo = smem_addr(stage_ptr(s, 3));
+            const uint32_t ah = smem_addr(tile(s, 0)), al = smem_addr(tile(s, 1));
+            const uint32_t bh = smem_addr(tile(s, 2)), bl = smem_addr(tile(s, 3));
 #pragma unroll
-            for (int it = 0; it < 12; ++it) {  // hi*hi, hi*lo, lo*hi over 4 steps of K = 16
+            for (int it = 0; it < 12; ++it) {
                 const int pass = it / 4, ks = it % 4;
-                const uint32_t A = (pass == 2 ? a_lo : a_hi) + ks * 32;
-                const uint32_t B = (pass == 1 ? b_lo : b_hi) + ks * 32;
+                const uint32_t A = (pass == 2 ? al : ah) + ks * 32;
+                const uint32_t B = (pass == 1 ? bl : bh) + ks * 32;
                 tc::mma_bf16(tmem, tc::desc_kmajor_sw128(A), tc::desc_kmajor_sw128(B), idesc, (i > 0 || it > 0) ? 1u : 0u);
             }
-            tc::commit(&bar[s]);
+            tc::commit(&empty[s]);
         }
-        if (i + 1 < nk) {
-            const int s2 = (i + 1) & 1;
-            if (i >= 1) ok &= mbar_wait_bounded(&bar[s2], ((i - 1) >> 1) & 1);  // slice i - 1 read by the MMAs
-            const int64_t k0 = kb + static_cast<int64_t>(i + 1) * kBK;
-            load_slice(g.a, g.amask, g.lda, g.vec_a, m0, g.M, k0, ke, stage_ptr(s2, 0), stage_ptr(s2, 1));
-            load_slice(g.b, nullptr, g.ldb, g.vec_b, n0, g.N, k0, ke, stage_ptr(s2, 2), stage_ptr(s2, 3));
-        }
+        tc::commit(done);  // every MMA issued above has completed when this arrives
     }
-    if (nk > 0) ok &= mbar_wait_bounded(&bar[(nk - 1) & 1], ((nk - 1) >> 1) & 1);
+    __syncwarp();
+    if (nk > 0) ok &= mbar_wait_bounded(done, 0);
     ok = __syncthreads_and(ok) != 0;
-    if (!ok) {
-        if (threadIdx.x == 0 && nk > 0) {
-            flag_status(g.status, DLRM_ERR_TIMEOUT);
-            (void)mbar_wait_bounded(&bar[(nk - 1) & 1], ((nk - 1) >> 1) & 1);  // the MMAs still in flight end first
-        }
-        __syncthreads();
-    }
+    if (!ok && threadIdx.x == 0) flag_status(g.status, DLRM_ERR_TIMEOUT);
     tc::fence_after_sync();
 
-    // epilogue: rows 32 (warp % 4) + lane, columns 64 (warp / 4) .. + 63
+    // epilogue: rows 32 warp + lane, the tile's 128 columns in four loads of 32
     if (ok) {
-        const int q = warp & 3, half = warp >> 2;
-        const int64_t m = m0 + 32 * q + lane;
+        const int64_t m = m0 + 32 * warp + lane;
         float* crow = g.c + static_cast<int64_t>(blockIdx.z) * g.split_stride + m * g.ldc;
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-            const int col0 = half * 64 + cb * 32;
+#pragma unroll 1
+        for (int cb = 0; cb < kBN / 32; ++cb) {
             uint32_t r[32];
-            tc::tmem_ld_32x32b_x32(tmem + ((static_cast<uint32_t>(32 * q)) << 16) + static_cast<uint32_t>(col0), r);
+            tc::tmem_ld_32x32b_x32(tmem + ((static_cast<uint32_t>(32 * warp)) << 16) + static_cast<uint32_t>(32 * cb), r);
             tc::tmem_ld_wait();
             if (nk == 0) {
 #pragma unroll
@@ -213,7 +165,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             if (m < g.M) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int64_t n = n0 + col0 + j;
+                    const int64_t n = n0 + 32 * cb + j;
                     if (n < g.N) {
                         float v = __uint_as_float(r[j]);
                         if (g.bias != nullptr) v += __ldg(g.bias + n);
@@ -232,18 +184,46 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     }
 }
 
-// out[c][r] = in[r][c] (times [mask[r][c] > 0] when a mask is given); in is R x C, out is C x R.
-__global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ in, const float* __restrict__ mask,
-                                                        float* __restrict__ out, int64_t R, int64_t C)
+// ---- operand preparation: fp32 -> bf16 hi / lo ---------------------------------------------------------
+__device__ __forceinline__ void split_one(float v, __nv_bfloat16& h, __nv_bfloat16& l)
+{
+    h = __float2bfloat16_rn(v);
+    l = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// hi / lo [R x Kp] of src [R x K] (leading dimension ld), times [mask > 0] when a mask is given; columns
+// K .. Kp - 1 are zero.
+__global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, const float* __restrict__ mask,
+                                                         int64_t ld, int64_t R, int64_t K, int64_t Kp,
+                                                         __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo)
+{
+    const int64_t n = R * Kp;
+    for (int64_t e = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; e < n; e += int64_t{gridDim.x} * blockDim.x) {
+        const int64_t r = e / Kp, k = e - r * Kp;
+        float v = 0.0f;
+        if (k < K) {
+            v = src[r * ld + k];
+            if (mask != nullptr && !(mask[r * ld + k] > 0.0f)) v = 0.0f;
+        }
+        split_one(v, hi[e], lo[e]);
+    }
+}
+
+// hi / lo [C x Rp] of the transpose of src [R x C] (times [mask > 0]); columns R .. Rp - 1 are zero.
+// 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src,
+                                                              const float* __restrict__ mask, int64_t R, int64_t C,
+                                                              int64_t Rp, __nv_bfloat16* __restrict__ hi,
+                                                              __nv_bfloat16* __restrict__ lo)
 {
     __shared__ float tile[32][33];
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     for (int j = ty; j < 32; j += 8) {
         const int64_t r = r0 + j, c = c0 + tx;
         float v = 0.0f;
         if (r < R && c < C) {
-            v = in[r * C + c];
+            v = src[r * C + c];
             if (mask != nullptr && !(mask[r * C + c] > 0.0f)) v = 0.0f;
         }
         tile[j][tx] = v;
@@ -251,30 +231,41 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict_
     __syncthreads();
     for (int j = ty; j < 32; j += 8) {
         const int64_t c = c0 + j, r = r0 + tx;
-        if (c < C && r < R) out[c * R + r] = tile[tx][j];
+        if (c < C && r < Rp) split_one(r < R ? tile[tx][j] : 0.0f, hi[c * Rp + r], lo[c * Rp + r]);
     }
 }
 
-// Row sums of X (rows x cols, cols contiguous), one block per row, a fixed reduction tree.
-__global__ void __launch_bounds__(256) row_sum_kernel(const float* __restrict__ x, int64_t cols, float* __restrict__ out)
+// Column sums of src [R x C] (times [mask > 0]) over row chunks: part[chunk][c]; a fixed order.
+constexpr int kColChunks = 64;
+__global__ void __launch_bounds__(256) col_sum_kernel(const float* __restrict__ src, const float* __restrict__ mask,
+                                                      int64_t R, int64_t C, float* __restrict__ part)
 {
-    __shared__ float part[256];
-    const float* row = x + static_cast<int64_t>(blockIdx.x) * cols;
+    __shared__ float acc[8][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + tx;
+    const int64_t per = (R + kColChunks - 1) / kColChunks;
+    const int64_t r_lo = static_cast<int64_t>(blockIdx.y) * per, r_hi = min(R, r_lo + per);
     float s = 0.0f;
-    for (int64_t c = threadIdx.x; c < cols; c += 256) s += row[c];
-    part[threadIdx.x] = s;
+    if (c < C)
+        for (int64_t r = r_lo + ty; r < r_hi; r += 8) {
+            float v = src[r * C + c];
+            if (mask != nullptr && !(mask[r * C + c] > 0.0f)) v = 0.0f;
+            s += v;
+        }
+    acc[ty][tx] = s;
     __syncthreads();
-    for (int w = 128; w > 0; w >>= 1) {
-        if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-        __syncthreads();
+    if (ty == 0 && c < C) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += acc[q][tx];
+        part[static_cast<int64_t>(blockIdx.y) * C + c] = t;
     }
-    if (threadIdx.x == 0) out[blockIdx.x] = part[0];
 }
 
-// W -= lr * sum_s partial[s] (splits added in order), b -= lr * db.
+// W -= lr * sum_s partial[s] (splits added in order); b -= lr * sum_chunk db_part[chunk] (in order).
 __global__ void __launch_bounds__(256) sgd_update_kernel(float* __restrict__ w, const float* __restrict__ partial,
                                                          int splits, int64_t n, float* __restrict__ b,
-                                                         const float* __restrict__ db, int64_t nb, float lr)
+                                                         const float* __restrict__ db_part, int64_t nb, float lr)
 {
     for (int64_t i = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; i < n; i += int64_t{gridDim.x} * blockDim.x) {
         float s = 0.0f;
@@ -282,8 +273,11 @@ __global__ void __launch_bounds__(256) sgd_update_kernel(float* __restrict__ w, 
         w[i] = fmaf(-lr, s, w[i]);
     }
     if (b != nullptr)
-        for (int64_t i = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; i < nb; i += int64_t{gridDim.x} * blockDim.x)
-            b[i] = fmaf(-lr, db[i], b[i]);
+        for (int64_t i = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; i < nb; i += int64_t{gridDim.x} * blockDim.x) {
+            float s = 0.0f;
+            for (int q = 0; q < kColChunks; ++q) s += db_part[static_cast<int64_t>(q) * nb + i];
+            b[i] = fmaf(-lr, s, b[i]);
+        }
 }
 
 // ---- head ----------------------------------------------------------------------------------------------
@@ -349,18 +343,28 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restr
     }
 }
 
-// Sums the blocks' partials in block order; loss = sum / M; w -= lr dw; b -= lr db.
+// Sums the blocks' partials in block order; loss = sum / M; w -= lr dw; b -= lr db.  A block per 32
+// columns of w: warp q adds blocks q, q + 8, ..., then the 8 warp sums are added in warp order.
 __global__ void __launch_bounds__(256) head_update_kernel(float* __restrict__ w, float* __restrict__ b,
                                                           const float* __restrict__ part_w,
                                                           const float* __restrict__ part_s, int blocks, int in_dim,
                                                           int64_t M, float lr, float* __restrict__ loss)
 {
-    for (int k = threadIdx.x; k < in_dim; k += blockDim.x) {
-        float s = 0.0f;
-        for (int q = 0; q < blocks; ++q) s += part_w[static_cast<int64_t>(q) * in_dim + k];
-        w[k] = fmaf(-lr, s, w[k]);
+    __shared__ float acc[8][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int k = blockIdx.x * 32 + tx;
+    float s = 0.0f;
+    if (k < in_dim)
+        for (int q = ty; q < blocks; q += 8) s += part_w[static_cast<int64_t>(q) * in_dim + k];
+    acc[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && k < in_dim) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += acc[q][tx];
+        w[k] = fmaf(-lr, t, w[k]);
     }
-    if (threadIdx.x == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         float db = 0.0f, l = 0.0f;
         for (int q = 0; q < blocks; ++q) {
             db += part_s[2 * q];
@@ -377,29 +381,65 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
 
 int splits_for(int64_t tiles, int64_t K)
 {
-    // enough CTAs for two per SM, each split at least 4 slices of K
+    // enough CTAs for one per SM (a CTA holds 192 KB of shared memory), each split at least 4 slices of K
     const int sms = sm_count();
-    int s = static_cast<int>((2 * static_cast<int64_t>(sms) + tiles - 1) / (tiles > 0 ? tiles : 1));
+    int s = static_cast<int>((static_cast<int64_t>(sms) + tiles - 1) / (tiles > 0 ? tiles : 1));
     const int64_t max_s = (K + 4 * kBK - 1) / (4 * kBK);
     if (s > max_s) s = static_cast<int>(max_s);
     return s < 1 ? 1 : s;
 }
 
-}  // namespace
+int64_t pad8(int64_t x) { return (x + 7) / 8 * 8; }
 
-dlrm_status launch_gemm(const float* a, const float* amask, int64_t lda, const float* b, int64_t ldb,
-                        const float* bias, float* c, int64_t ldc, int64_t M, int64_t N, int64_t K, int relu,
-                        int splits, int64_t split_stride, int32_t* status, cudaStream_t s)
+// cuTensorMapEncodeTiled, resolved once through the runtime (a driver function, the same for every device).
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encoder()
+{
+    static std::atomic<void*> fn{nullptr};
+    void* f = fn.load(std::memory_order_acquire);
+    if (f == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<EncodeFn>(f);
+}
+
+// A bf16 [rows x kp] row-major operand, tiles of 64 (K) x 128 rows, 128-byte swizzle, zero fill out of range.
+bool encode_operand(CUtensorMap* map, const __nv_bfloat16* base, int64_t rows, int64_t kp)
+{
+    EncodeFn enc = encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kp) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// C = A B^T from split operands: A hi / lo [M x kp], B hi / lo [N x kp], K the reduction length (<= kp).
+dlrm_status launch_gemm(const __nv_bfloat16* ah, const __nv_bfloat16* al, const __nv_bfloat16* bh,
+                        const __nv_bfloat16* bl, int64_t kp, const float* bias, float* c, int64_t ldc, int64_t M,
+                        int64_t N, int64_t K, int relu, int splits, int64_t split_stride, int32_t* status,
+                        cudaStream_t s)
 {
     if (M <= 0 || N <= 0) return DLRM_OK;
+    if (M > INT32_MAX || N > INT32_MAX || kp > INT32_MAX) return DLRM_ERR_UNSUPPORTED;
     GemmArgs g;
-    g.a = a;
-    g.amask = amask;
-    g.b = b;
+    memset(&g, 0, sizeof g);
+    if (!encode_operand(&g.a_hi, ah, M, kp) || !encode_operand(&g.a_lo, al, M, kp) ||
+        !encode_operand(&g.b_hi, bh, N, kp) || !encode_operand(&g.b_lo, bl, N, kp))
+        return DLRM_ERR_CUDA;
     g.bias = bias;
     g.c = c;
-    g.lda = lda;
-    g.ldb = ldb;
     g.ldc = ldc;
     g.M = M;
     g.N = N;
@@ -408,9 +448,6 @@ dlrm_status launch_gemm(const float* a, const float* amask, int64_t lda, const f
     g.k_per_split = (per + kBK - 1) / kBK * kBK;
     g.split_stride = split_stride;
     g.relu = relu;
-    g.vec_a = (lda % 4 == 0) && ((reinterpret_cast<uintptr_t>(a) & 15u) == 0) &&
-              (amask == nullptr || (reinterpret_cast<uintptr_t>(amask) & 15u) == 0);
-    g.vec_b = (ldb % 4 == 0) && ((reinterpret_cast<uintptr_t>(b) & 15u) == 0);
     g.status = status;
     if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) != cudaSuccess)
         return DLRM_ERR_CUDA;
@@ -420,62 +457,133 @@ dlrm_status launch_gemm(const float* a, const float* amask, int64_t lda, const f
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
+// Carves bf16 hi / lo pairs and fp32 arrays out of a workspace, 256-byte aligned.
+struct Carver {
+    char* p;
+    size_t used = 0;
+    template <typename T>
+    T* take(size_t count)
+    {
+        T* at = p ? reinterpret_cast<T*>(p + used) : nullptr;
+        used = align256(used + sizeof(T) * count);
+        return at;
+    }
+};
+
+void split_rows(const float* src, const float* mask, int64_t ld, int64_t R, int64_t K, int64_t Kp, __nv_bfloat16* hi,
+                __nv_bfloat16* lo, cudaStream_t s)
+{
+    const int64_t n = R * Kp;
+    const int64_t blocks = (n + 255) / 256;
+    split_rows_kernel<<<static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, s>>>(src, mask, ld, R, K,
+                                                                                                   Kp, hi, lo);
+}
+
+void split_transpose(const float* src, const float* mask, int64_t R, int64_t C, int64_t Rp, __nv_bfloat16* hi,
+                     __nv_bfloat16* lo, cudaStream_t s)
+{
+    const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((Rp + 31) / 32));
+    split_transpose_kernel<<<grid, 256, 0, s>>>(src, mask, R, C, Rp, hi, lo);
+}
+
+// Workspace of the forward: x and W split.
+struct FwdWs {
+    __nv_bfloat16 *xh, *xl, *wh, *wl;
+};
+FwdWs carve_fwd(void* base, int64_t M, int32_t K, int32_t N, size_t* bytes)
+{
+    Carver c{static_cast<char*>(base)};
+    const int64_t kp = pad8(K);
+    FwdWs w;
+    w.xh = c.take<__nv_bfloat16>(M * kp);
+    w.xl = c.take<__nv_bfloat16>(M * kp);
+    w.wh = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * kp);
+    w.wl = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * kp);
+    if (bytes) *bytes = c.used;
+    return w;
+}
+
+// Workspace of the backward: dz and W^T split (dx), dz^T and x^T split (dW), the dW partials, the db partials.
+struct BwdWs {
+    __nv_bfloat16 *dzh, *dzl, *wth, *wtl, *dzth, *dztl, *xth, *xtl;
+    float *part, *db_part;
+    int splits;
+};
+BwdWs carve_bwd(void* base, int64_t M, int32_t K, int32_t N, size_t* bytes)
+{
+    Carver c{static_cast<char*>(base)};
+    const int64_t np = pad8(N), mp = pad8(M);
+    BwdWs w;
+    const int64_t tiles = ((N + kBM - 1) / kBM) * ((K + kBN - 1) / kBN);
+    w.splits = splits_for(tiles, M);
+    w.dzh = c.take<__nv_bfloat16>(M * np);
+    w.dzl = c.take<__nv_bfloat16>(M * np);
+    w.wth = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * np);
+    w.wtl = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * np);
+    w.dzth = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * mp);
+    w.dztl = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * mp);
+    w.xth = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * mp);
+    w.xtl = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * mp);
+    w.part = c.take<float>(static_cast<size_t>(w.splits) * N * K);
+    w.db_part = c.take<float>(static_cast<size_t>(kColChunks) * N);
+    if (bytes) *bytes = c.used;
+    return w;
+}
+
+}  // namespace
+
+size_t fc_fwd_workspace_bytes(int64_t M, int32_t K, int32_t N)
+{
+    size_t b = 0;
+    carve_fwd(nullptr, M, K, N, &b);
+    return b;
+}
+
 size_t fc_bwd_workspace_bytes(int64_t M, int32_t K, int32_t N)
 {
-    const int64_t tiles = ((N + kBN - 1) / kBN) * ((K + kBN - 1) / kBN);
-    const int splits = splits_for(tiles, M);
-    return align256(sizeof(float) * static_cast<size_t>(K) * N)            // W^T
-           + align256(sizeof(float) * static_cast<size_t>(N) * M)          // dz^T
-           + align256(sizeof(float) * static_cast<size_t>(K) * M)          // x^T
-           + align256(sizeof(float) * static_cast<size_t>(splits) * N * K) // dW partials
-           + align256(sizeof(float) * static_cast<size_t>(N));             // db
+    size_t b = 0;
+    carve_bwd(nullptr, M, K, N, &b);
+    return b;
 }
 
 dlrm_status launch_fc_fwd(const float* x, const float* w, const float* b, int64_t M, int32_t K, int32_t N, int relu,
-                          float* y, int32_t* status, cudaStream_t s)
+                          float* y, void* workspace, int32_t* status, cudaStream_t s)
 {
-    return launch_gemm(x, nullptr, K, w, K, b, y, N, M, N, K, relu, 1, 0, status, s);
+    const FwdWs ws = carve_fwd(workspace, M, K, N, nullptr);
+    const int64_t kp = pad8(K);
+    split_rows(x, nullptr, K, M, K, kp, ws.xh, ws.xl, s);
+    split_rows(w, nullptr, K, N, K, kp, ws.wh, ws.wl, s);
+    return launch_gemm(ws.xh, ws.xl, ws.wh, ws.wl, kp, b, y, N, M, N, K, relu, 1, 0, status, s);
 }
 
 dlrm_status launch_fc_bwd_sgd(const float* x, float* w, float* b, const float* y, const float* dy, int64_t M, int32_t K,
                               int32_t N, int relu, float lr, float* dx, void* workspace, int32_t* status,
                               cudaStream_t s)
 {
-    const int64_t tiles = ((N + kBN - 1) / kBN) * ((K + kBN - 1) / kBN);
-    const int splits = splits_for(tiles, M);
-    char* p = static_cast<char*>(workspace);
-    float* wt = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * static_cast<size_t>(K) * N);
-    float* dzt = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * static_cast<size_t>(N) * M);
-    float* xt = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * static_cast<size_t>(K) * M);
-    float* part = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * static_cast<size_t>(splits) * N * K);
-    float* db = reinterpret_cast<float*>(p);
+    const BwdWs ws = carve_bwd(workspace, M, K, N, nullptr);
+    const int64_t np = pad8(N), mp = pad8(M);
     const float* mask = relu ? y : nullptr;
-
-    auto transpose = [&](const float* in, const float* msk, float* out, int64_t R, int64_t C) {
-        const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((R + 31) / 32));
-        transpose_kernel<<<grid, 256, 0, s>>>(in, msk, out, R, C);
-    };
-    // dx = dz W = dz (W^T)^T, with the ReLU mask applied to dz while it is loaded
+    // dx = dz W: A = dz [M x N] (mask applied), B = W^T [K x N]
     if (dx != nullptr) {
-        transpose(w, nullptr, wt, N, K);
-        dlrm_status st = launch_gemm(dy, mask, N, wt, N, nullptr, dx, K, M, K, N, 0, 1, 0, status, s);
+        split_rows(dy, mask, N, M, N, np, ws.dzh, ws.dzl, s);
+        split_transpose(w, nullptr, N, K, np, ws.wth, ws.wtl, s);
+        dlrm_status st = launch_gemm(ws.dzh, ws.dzl, ws.wth, ws.wtl, np, nullptr, dx, K, M, K, N, 0, 1, 0, status, s);
         if (st != DLRM_OK) return st;
     }
-    // dW = dz^T x over the batch, in split partials; db = row sums of dz^T
-    transpose(dy, mask, dzt, M, N);
-    transpose(x, nullptr, xt, M, K);
-    dlrm_status st = launch_gemm(dzt, nullptr, M, xt, M, nullptr, part, K, N, K, M, 0, splits,
+    // dW = dz^T x over the batch, in split partials: A = dz^T [N x M], B = x^T [K x M]
+    split_transpose(dy, mask, M, N, mp, ws.dzth, ws.dztl, s);
+    split_transpose(x, nullptr, M, K, mp, ws.xth, ws.xtl, s);
+    dlrm_status st = launch_gemm(ws.dzth, ws.dztl, ws.xth, ws.xtl, mp, nullptr, ws.part, K, N, K, M, 0, ws.splits,
                                  static_cast<int64_t>(N) * K, status, s);
     if (st != DLRM_OK) return st;
-    row_sum_kernel<<<static_cast<unsigned>(N), 256, 0, s>>>(dzt, M, db);
+    if (b != nullptr) {
+        const dim3 grid(static_cast<unsigned>((N + 31) / 32), kColChunks);
+        col_sum_kernel<<<grid, 256, 0, s>>>(dy, mask, M, N, ws.db_part);
+    }
     const int64_t n = static_cast<int64_t>(N) * K;
     const int64_t blocks = (n + 255) / 256;
-    sgd_update_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(w, part, splits, n, b, db,
-                                                                                          b != nullptr ? N : 0, lr);
+    sgd_update_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
+        w, ws.part, ws.splits, n, b, ws.db_part, b != nullptr ? N : 0, lr);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
@@ -496,7 +604,8 @@ dlrm_status launch_head(const float* h, float* w, float* b, const float* label, 
                                              align256(sizeof(float) * static_cast<size_t>(blocks) * K));
     head_kernel<<<static_cast<unsigned>(blocks), kHeadThreads, 0, s>>>(h, w, b, label, M, K, kHeadRowsPerBlock, prob,
                                                                        dh, part_w, part_s);
-    head_update_kernel<<<1, 256, 0, s>>>(w, b, part_w, part_s, static_cast<int>(blocks), K, M, lr, loss);
+    head_update_kernel<<<static_cast<unsigned>((K + 31) / 32), 256, 0, s>>>(w, b, part_w, part_s,
+                                                                            static_cast<int>(blocks), K, M, lr, loss);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 

@@ -369,15 +369,21 @@ dlrm_status dlrm_tier_stage(const dlrm_tiered_tables *tables, const dlrm_bags *b
  * products run on the tcgen05 tensor cores with each fp32 operand split into
  * two bf16 values (hi + lo; hi*hi + hi*lo + lo*hi accumulated in fp32), which
  * keeps about 16 significant bits of every product (relative error below
- * 2^-16 of sum |a_k b_k|).  All matrices row-major, device memory, 16-byte
+ * 2^-16 of sum |a_k b_k|).  The split copies go to the caller's workspace;
+ * the tensor cores read them through TMA tile loads.  All matrices row-major, device memory, 16-byte
  * aligned; W is out_dim x in_dim (y = x W^T + b). */
 typedef enum { DLRM_ACT_NONE = 0, DLRM_ACT_RELU = 1 } dlrm_activation;
 
+/* Bytes of device workspace dlrm_fc_fwd needs (bf16 hi / lo copies of x and W). */
+dlrm_status dlrm_fc_fwd_workspace_size(int64_t batch, int32_t in_dim, int32_t out_dim, size_t *bytes);
+
 /* y[batch][out_dim] = act(x[batch][in_dim] W^T + b); b may be NULL (no bias).
- * in_dim, out_dim in [1, 65536], batch in [1, 2^31]. */
+ * in_dim, out_dim in [1, 65536], batch in [1, 2^31 - 1].  workspace: device,
+ * at least dlrm_fc_fwd_workspace_size() bytes, 16-byte aligned. */
 dlrm_status dlrm_fc_fwd(const float *x, const float *w, const float *b, int64_t batch,
                         int32_t in_dim, int32_t out_dim, int32_t act, float *y,
-                        int32_t *status_dev, cudaStream_t stream);
+                        void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                        cudaStream_t stream);
 
 /* Bytes of device workspace dlrm_fc_bwd_sgd needs. */
 dlrm_status dlrm_fc_bwd_workspace_size(int64_t batch, int32_t in_dim, int32_t out_dim, size_t *bytes);
