@@ -665,36 +665,123 @@ __device__ __forceinline__ void adagrad_apply(const BwdArgs& a, uint32_t key, in
     if (lane == 0) a.accum[t][r] = A;
 }
 
-// Per group of U sorted lookups the warp issues, together, the loads of the
-// group's dP rows and of the weights and accumulator of every row whose run
-// starts in the group (each row is updated once per call, so reading it early
-// is safe), then walks the group in order.
+// Shared-memory copies (cp.async: global -> shared without a register stop).
+// A lane reads back only the bytes it copied itself (the accumulator aside),
+// so its own cp.async.wait_group is the only wait the ring needs.
+__device__ __forceinline__ void seg_copy16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void seg_copy4(void* dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void seg_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void seg_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// The per-row sums keep kDepth - 1 lookups in flight per warp: each lookup's
+// dP row and, where a run starts, its row's weights and accumulator travel
+// into a ring of kDepth shared-memory slots while the warp walks earlier
+// lookups.  A slot is refilled one lookup after it was read.
 template <int D>
-__global__ void __launch_bounds__(kSegThreads, D >= 256 ? 4 : 8) segment_chunk_kernel(const __grid_constant__ BwdArgs a,
-                                                                       const uint32_t* __restrict__ keys,
-                                                                       const uint32_t* __restrict__ vals,
-                                                                       const float* __restrict__ dP,
-                                                                       float* __restrict__ partial, int64_t num_chunks)
+struct alignas(16) SegRing {
+    static constexpr int kDepth = 5;
+    static constexpr int kMinBlocks = D >= 256 ? 4 : 8;  // CTAs of 4 warps per SM (shared memory, registers)
+    static constexpr uint8_t kNoRun = 0xFF;                 // table[] of a lookup that starts no run
+    float drow[kDepth][D];   // dP rows
+    float wrow[kDepth][D];   // weights of the rows whose runs start at these lookups
+    float acc[kDepth];       // their accumulators (Adagrad)
+    uint32_t key[kChunk];    // the chunk's sorted lookups
+    uint32_t val[kChunk];
+    uint8_t table[kChunk];   // the table of a run's row at the run's first lookup, kNoRun elsewhere
+};
+
+template <int D>
+constexpr size_t seg_smem_bytes()
+{
+    return sizeof(SegRing<D>) * (kSegThreads / kWarp);
+}
+
+// One warp per chunk.  The chunk is staged once, lane-parallel: keys, values
+// and, at each lookup whose key differs from the one before (a run starts),
+// the table of its row.  Then the warp walks the lookups in order, adds each
+// dP row into the running sum of its run and updates the row when the run
+// ends inside the chunk.
+template <int D>
+__global__ void __launch_bounds__(kSegThreads, SegRing<D>::kMinBlocks) segment_chunk_kernel(
+    const __grid_constant__ BwdArgs a, const uint32_t* __restrict__ keys, const uint32_t* __restrict__ vals,
+    const float* __restrict__ dP, float* __restrict__ partial, int64_t num_chunks)
 {
     constexpr int C = Lanes<D>::kChunks;
-    constexpr int U = 2;  // lookups per group: small, since more warps per SM (8 CTAs) hide this kernel's
-                          // chains of dependent instructions better than deeper loads do
+    constexpr int R = SegRing<D>::kDepth;
+    constexpr uint8_t kNoRun = SegRing<D>::kNoRun;
+    extern __shared__ __align__(16) unsigned char seg_smem[];
     const int lane = threadIdx.x & 31;
     const int64_t chunk = blockIdx.x * int64_t{blockDim.x / kWarp} + (threadIdx.x >> 5);
     if (chunk >= num_chunks) return;
+    SegRing<D>& ring = reinterpret_cast<SegRing<D>*>(seg_smem)[threadIdx.x >> 5];
     const bool active = lane < Lanes<D>::kActive;
     const int64_t c0 = chunk * kChunk;
-    const int64_t c1 = min(c0 + kChunk, a.nnz);
+    const int n = static_cast<int>(min(static_cast<int64_t>(kChunk), a.nnz - c0));
     const uint32_t before_key = c0 > 0 ? keys[c0 - 1] : kSentinel;
-    const uint32_t after_key = c1 < a.nnz ? keys[c1] : kSentinel;
+    const uint32_t after_key = c0 + n < a.nnz ? keys[c0 + n] : kSentinel;
+
+    // lookups that update nothing (sentinel keys) sort last, so the live ones are a prefix
+    int live = 0;
+    uint32_t prev = before_key;
+    for (int i0 = 0; i0 < n; i0 += kWarp) {
+        const int i = i0 + lane;
+        const uint32_t k = i < n ? keys[c0 + i] : kSentinel;
+        const uint32_t v = i < n ? vals[c0 + i] : 0u;
+        uint32_t kp = __shfl_up_sync(0xffffffffu, k, 1);
+        if (lane == 0) kp = prev;
+        prev = __shfl_sync(0xffffffffu, k, kWarp - 1);
+        if (i < n) {
+            ring.key[i] = k;
+            ring.val[i] = v;
+            ring.table[i] = k != kSentinel && k != kp
+                                ? static_cast<uint8_t>(v - div_by_T(v, a) * static_cast<uint32_t>(a.T))
+                                : kNoRun;
+        }
+        live += __popc(__ballot_sync(0xffffffffu, k != kSentinel));
+    }
+    __syncwarp();
+
+    auto issue = [&](int j, int slot) {
+        if (j < live) {
+            if (active) {
+                const float* src = dP + static_cast<int64_t>(ring.val[j]) * D;
+#pragma unroll
+                for (int q = 0; q < C; ++q) {
+                    const int col = (lane + q * kWarp) * 4;
+                    seg_copy16(&ring.drow[slot][col], src + col);
+                }
+            }
+            const int t = ring.table[j];
+            if (t != kNoRun) {  // a run starts here: its row's weights and accumulator too
+                const int64_t r = static_cast<int64_t>(ring.key[j]) - a.row_base[t];
+                if (active) {
+                    const float* wr = a.tables[t] + r * D;
+#pragma unroll
+                    for (int q = 0; q < C; ++q) {
+                        const int col = (lane + q * kWarp) * 4;
+                        seg_copy16(&ring.wrow[slot][col], wr + col);
+                    }
+                }
+                if (lane == 0 && a.rule == DLRM_RULE_ADAGRAD) seg_copy4(&ring.acc[slot], a.accum[t] + r);
+            }
+        }
+        seg_commit();  // one group per lookup, empty past the end, so the wait below counts lookups
+    };
 
     uint32_t cur = kSentinel;
     int cur_t = 0;
     bool cur_first = true;  // current run is the chunk's first run
-    float4 g[C], cw[C];     // the run's gradient sum; its row's weights (read at the run's start)
+    float4 g[C], cw[C];     // the run's gradient sum; its row's weights
     float ca = 0.0f;        // its accumulator
 #pragma unroll
-    for (int k = 0; k < C; ++k) g[k] = cw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < C; ++q) g[q] = cw[q] = make_float4(0.f, 0.f, 0.f, 0.f);
 
     auto flush = [&]() {
         if (cur == kSentinel) return;
@@ -706,72 +793,44 @@ __global__ void __launch_bounds__(kSegThreads, D >= 256 ? 4 : 8) segment_chunk_k
             float* dst = partial + ((chunk * 2) + (cur_first ? 0 : 1)) * D;
             if (active) {
 #pragma unroll
-                for (int k = 0; k < C; ++k) *reinterpret_cast<float4*>(dst + (lane + k * kWarp) * 4) = g[k];
+                for (int q = 0; q < C; ++q) *reinterpret_cast<float4*>(dst + (lane + q * kWarp) * 4) = g[q];
             }
         }
     };
 
-    uint32_t prev_key = before_key;  // key of the lookup before the current group
-    for (int64_t base = c0; base < c1; base += kWarp) {
-        const int64_t p = base + lane;
-        const uint32_t kk = p < c1 ? keys[p] : kSentinel;
-        const uint32_t vv = p < c1 ? vals[p] : 0u;
-        const int nq = static_cast<int>(c1 - base < kWarp ? c1 - base : kWarp);
-        for (int j0 = 0; j0 < nq; j0 += U) {
-            float4 row[U][C], wp[U][C];
-            float ap[U];
-            uint32_t kj[U];
-            int tj[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = j0 + u;
-                kj[u] = __shfl_sync(0xffffffffu, kk, j & 31);
-                const uint32_t vj = __shfl_sync(0xffffffffu, vv, j & 31);
-                if (j >= nq) kj[u] = kSentinel;
-                const uint32_t kprev = u == 0 ? prev_key : kj[u - 1];
-                tj[u] = 0;
-                if (kj[u] != kSentinel) {
-                    if (active) {
-                        const float* src = dP + static_cast<int64_t>(vj) * D;
-#pragma unroll
-                        for (int k = 0; k < C; ++k) row[u][k] = *reinterpret_cast<const float4*>(src + (lane + k * kWarp) * 4);
-                    }
-                    if (kj[u] != kprev) {  // a run starts here: read its row now
-                        const uint32_t b = div_by_T(vj, a);
-                        tj[u] = static_cast<int>(vj - b * static_cast<uint32_t>(a.T));
-                        const int64_t r = static_cast<int64_t>(kj[u]) - a.row_base[tj[u]];
-                        ap[u] = a.rule == DLRM_RULE_ADAGRAD ? a.accum[tj[u]][r] : 0.0f;
-                        if (active) {
-                            const float* wr = a.tables[tj[u]] + r * D;
-#pragma unroll
-                            for (int k = 0; k < C; ++k) wp[u][k] = *reinterpret_cast<const float4*>(wr + (lane + k * kWarp) * 4);
-                        }
-                    }
+    for (int j = 0; j < R - 1; ++j) issue(j, j);
+    int rs = 0, ws = R - 1;  // the slot read now, the slot refilled now
+    for (int j = 0; j < live; ++j) {
+        seg_wait<R - 2>();  // this lookup's group has landed
+        const int t = ring.table[j];
+        if (t != kNoRun || j == 0) {  // a run starts (j == 0 may continue a run cut at the chunk's start)
+            flush();
+            cur_first = j == 0;
+            cur = ring.key[j];
+            cur_t = t;
+            if (t != kNoRun) {
+                if (a.rule == DLRM_RULE_ADAGRAD) {
+                    __syncwarp();  // lane 0's accumulator copy, landed, is seen by the warp
+                    ca = ring.acc[rs];
+                    __syncwarp();  // and read by every lane before lane 0 refills the slot
                 }
+#pragma unroll
+                for (int q = 0; q < C; ++q)
+                    if (active) cw[q] = *reinterpret_cast<const float4*>(&ring.wrow[rs][(lane + q * kWarp) * 4]);
             }
-            prev_key = kj[U - 1] != kSentinel ? kj[U - 1] : prev_key;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (kj[u] == kSentinel) continue;
-                if (kj[u] != cur) {
-                    flush();
-                    cur_first = (cur == kSentinel);
-                    cur = kj[u];
-                    cur_t = tj[u];
-                    ca = ap[u];
-#pragma unroll
-                    for (int k = 0; k < C; ++k) {
-                        g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        cw[k] = wp[u][k];
-                    }
-                }
-                if (active) {
-#pragma unroll
-                    for (int k = 0; k < C; ++k) add4(g[k], row[u][k]);
-                }
-            }
+            for (int q = 0; q < C; ++q) g[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        if (active) {
+#pragma unroll
+            for (int q = 0; q < C; ++q) add4(g[q], *reinterpret_cast<const float4*>(&ring.drow[rs][(lane + q * kWarp) * 4]));
+        }
+        issue(j + R - 1, ws);  // refills the slot read one lookup ago
+        rs = rs + 1 == R ? 0 : rs + 1;
+        ws = ws + 1 == R ? 0 : ws + 1;
     }
+    seg_wait<0>();
     flush();
 }
 
@@ -963,8 +1022,13 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const
     if (st != DLRM_OK || a.nnz == 0) return st;
 
     const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + kSegThreads / kWarp - 1) / (kSegThreads / kWarp));
-    segment_chunk_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], dP, w.partial,
-                                                               w.num_chunks);
+    constexpr size_t seg_smem = seg_smem_bytes<D>();
+    if (seg_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(segment_chunk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(seg_smem)) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+    segment_chunk_kernel<D><<<seg_blocks, kSegThreads, seg_smem, s>>>(a, w.keys[cur], w.vals[cur], dP, w.partial,
+                                                                      w.num_chunks);
     segment_span_kernel<D><<<seg_blocks, kSegThreads, 0, s>>>(a, w.keys[cur], w.vals[cur], w.partial, w.num_chunks);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
