@@ -722,7 +722,9 @@ def launches_per_step(args, w, plan=None) -> int:
                 n += 4 + 3 * passes_for_rows(rows) + (1 if w.mode == "mean" else 0)
         return n
     bwd = 5 + 3 * sort_passes(w)  # interaction backward, key fill and expansion, 3 per radix pass, 2 row updates
-    return n + 1 + (bwd if w.train and args.op == "fused" else 0)
+    if args.op != "fused":
+        return n + 1
+    return n + forward_launches(w) + (bwd if w.train else 0)
 
 
 def phase_is_traced(args, phase) -> bool:
@@ -786,8 +788,17 @@ def forward_kernel_name(w):
     tc = w.D in (64, 128) and w.T + 1 <= 128 and mean_len <= 16
     if not tc:
         return "forward_kernel (fused sparse forward, FFMA Gram" + (", two warps per sample)" if mean_len >= 8 else ")")
+    if w.train and mean_len > 1.25:
+        return ("embbag_list_kernel (lookup, pooled vectors saved for the backward) + forward_tc_kernel "
+                "(tcgen05 Gram on the saved vectors)")
     return ("forward_tc_kernel (fused sparse forward, tcgen05 Gram"
             + (", multi-lookup bags)" if mean_len > 1.25 else ")"))
+
+
+def forward_launches(w) -> int:
+    """Kernels of one forward: the training forward of multi-lookup bags is the lookup, then the
+    interaction on the saved pooled vectors; every other forward is one kernel."""
+    return 2 if forward_kernel_name(w).startswith("embbag_list_kernel") else 1
 
 
 def run_e2e_train(args, w, tables, batches, dev, dl, torch, world, side):

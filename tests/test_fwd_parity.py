@@ -116,6 +116,13 @@ def test_fused_multi_tile(case, orc):
     assert_close(o, ref["out"], ref["out_abs"], TOL_INTERACT if dtype == "f32" else TOL_BF16, "fused out")
     assert_close(pooled_save.cpu().numpy(), pooled_ref, pabs, TOL_BF16 if dtype == "bf16" else TOL_POOL_F32,
                  "fused pooled_save")
+    # without pooled_save the multi-lookup bags stay in the one fused kernel (with it, the lookup kernel
+    # writes the pooled vectors and the interaction reads them back): both routes against the oracle
+    out_inf = dl.dlrm_sparse_fwd(dt, di, do, torch.from_numpy(dense).cuda(), mode, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert_close(out_inf.cpu().numpy(), ref["out"], ref["out_abs"], TOL_INTERACT if dtype == "f32" else TOL_BF16,
+                 "fused out without pooled_save")
 
 
 def test_onehot_fp32_bit_exact(orc):
