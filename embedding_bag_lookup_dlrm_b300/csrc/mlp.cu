@@ -5,24 +5,22 @@
 // with ReLU, a sigmoid output; the hardware paragraph: the MLPs are ordinary
 // GEMMs on the tensor cores).
 //
-// GEMM.  C[M x N] = A[M x K] * B[N x K]^T with both operands K-major in global
-// memory (a row of A or B holds its K values contiguously), on the tcgen05
-// tensor cores: a CTA of 256 threads owns a 128 x 64 tile of C, walks K in
-// slices of 64, double-buffered in shared memory (96 KB: two CTAs per SM).  The
-// threads load a slice of fp32 A and B rows into registers (16-byte loads where
-// the rows allow), split each value v into bf16 hi = bf16(v) and lo =
-// bf16(v - hi) and store both into K-major 128-byte-swizzled operand buffers;
-// one thread issues hi*hi^T + hi*lo^T + lo*hi^T (3 x 4 MMAs of 128 x 64 x 16)
-// into a 64-column fp32 accumulator in TMEM and commits them to the slice's
-// mbarrier; the next slice's loads are issued right after, so they travel while
-// the MMAs run.  The dropped lo*lo term and the rounding of lo stay below 2^-16
-// relative to sum |a_k b_k|.  Epilogue: warp w reads TMEM lanes
-// 32 (w % 4) .. + 31 (rows of C), columns 32 (w / 4) .. + 31, adds the bias and
-// applies ReLU, or writes a split-K partial.
+// GEMM.  C[M x N] = A[M x K] * B[N x K]^T with both operands K-major (a row of
+// A or B holds its K values contiguously), on the tcgen05 tensor cores.  Each
+// fp32 operand is first split once into bf16 hi = bf16(v) and lo = bf16(v - hi)
+// arrays (K padded to a multiple of 8).  A CTA of 128 threads owns a 128 x 128
+// tile of C: one thread issues cp.async.bulk.tensor loads of 64-wide K slices
+// (128-byte swizzle, A hi / lo and B hi / lo, 64 KB) into a ring of 3 stages,
+// another issues hi*hi^T + hi*lo^T + lo*hi^T (12 MMAs of 128 x 128 x 16 per
+// slice) into a 128-column fp32 accumulator in TMEM and frees each stage by
+// commit.  The dropped lo*lo term and the rounding of lo stay below 2^-16
+// relative to sum |a_k b_k|.  Epilogue: all four warps read their 32 rows of the
+// accumulator, add the bias and apply ReLU (or write a split-K partial), and
+// store through a transpose in shared memory so that stores are row-contiguous.
 //
 // Backward of y = act(x W^T + b) from dy: dz = dy * [y > 0] (ReLU) or dy;
 // dx = dz W; dW = dz^T x; db = sum over the batch of dz.  dx is a GEMM with A =
-// dz (the mask applied while A is loaded) and B = W^T (an explicit transpose of
+// dz (the mask applied while dz is split) and B = W^T (an explicit transpose of
 // the small W); dW is a GEMM over the batch with A = dz^T and B = x^T (tiled
 // transposes through shared memory, the mask applied in the transpose), split
 // over the batch into partial sums that the update kernel adds in a fixed order
@@ -149,31 +147,36 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     if (!ok && threadIdx.x == 0) flag_status(g.status, DLRM_ERR_TIMEOUT);
     tc::fence_after_sync();
 
-    // epilogue: rows 32 warp + lane, the tile's 128 columns in four loads of 32
+    // epilogue: warp w reads rows 32 w + lane of the accumulator, 32 columns at a time, and passes them
+    // through a 32 x 33 transpose in the (now idle) operand ring, so that each store instruction writes 32
+    // consecutive columns of one row of C
     if (ok) {
-        const int64_t m = m0 + 32 * warp + lane;
-        float* crow = g.c + static_cast<int64_t>(blockIdx.z) * g.split_stride + m * g.ldc;
+        tc::fence_smem_for_mma();  // the ring was last read by the MMAs (async proxy)
+        float* stage = reinterpret_cast<float*>(sm) + warp * (32 * 33);
+        float* cbase = g.c + static_cast<int64_t>(blockIdx.z) * g.split_stride;
+        const int64_t mw = m0 + 32 * warp;
 #pragma unroll 1
         for (int cb = 0; cb < kBN / 32; ++cb) {
             uint32_t r[32];
             tc::tmem_ld_32x32b_x32(tmem + ((static_cast<uint32_t>(32 * warp)) << 16) + static_cast<uint32_t>(32 * cb), r);
             tc::tmem_ld_wait();
-            if (nk == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;  // an empty reduction range contributes zero
-            }
-            if (m < g.M) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int64_t n = n0 + 32 * cb + j;
-                    if (n < g.N) {
-                        float v = __uint_as_float(r[j]);
-                        if (g.bias != nullptr) v += __ldg(g.bias + n);
-                        if (g.relu) v = fmaxf(v, 0.0f);
-                        crow[n] = v;
-                    }
+            for (int j = 0; j < 32; ++j)  // an empty reduction range contributes zero
+                stage[lane * 33 + j] = nk == 0 ? 0.0f : __uint_as_float(r[j]);
+            __syncwarp();
+            const int64_t n = n0 + 32 * cb + lane;
+            const bool col = n < g.N;
+            const float bias = (col && g.bias != nullptr) ? __ldg(g.bias + n) : 0.0f;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(32), g.M - mw));
+            for (int i = 0; i < rows; ++i) {
+                if (col) {
+                    float v = stage[i * 33 + lane];
+                    if (g.bias != nullptr) v += bias;
+                    if (g.relu) v = fmaxf(v, 0.0f);
+                    cbase[(mw + i) * g.ldc + n] = v;
                 }
             }
+            __syncwarp();  // the stage is rewritten by the next column block
         }
     }
     tc::fence_before_sync();
@@ -191,35 +194,72 @@ __device__ __forceinline__ void split_one(float v, __nv_bfloat16& h, __nv_bfloat
     l = __float2bfloat16_rn(v - __bfloat162float(h));
 }
 
-// hi / lo [R x Kp] of src [R x K] (leading dimension ld), times [mask > 0] when a mask is given; columns
-// K .. Kp - 1 are zero.
+// hi and lo of 8 values as two 16-byte words of bf16 pairs.
+__device__ __forceinline__ void split8(const float (&v)[8], uint4& h, uint4& l)
+{
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        split_one(v[2 * i], h0, l0);
+        split_one(v[2 * i + 1], h1, l1);
+        hw[i] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+        lw[i] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+    }
+    h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    l = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// hi / lo [R x Kp] of src [R x K] (leading dimension ld), times [mask > 0] when a mask (same layout) is
+// given; columns K .. Kp - 1 are zero.  A thread splits 8 consecutive columns of a row (Kp is a multiple of
+// 8) and stores 16 bytes of hi and 16 of lo; vec: rows start 16-byte aligned, so full groups load as float4.
 __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict__ src, const float* __restrict__ mask,
-                                                         int64_t ld, int64_t R, int64_t K, int64_t Kp,
+                                                         int64_t ld, int64_t R, int64_t K, int64_t Kp, int vec,
                                                          __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo)
 {
-    const int64_t n = R * Kp;
+    const int64_t groups = Kp / 8;
+    const int64_t n = R * groups;
     for (int64_t e = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; e < n; e += int64_t{gridDim.x} * blockDim.x) {
-        const int64_t r = e / Kp, k = e - r * Kp;
-        float v = 0.0f;
-        if (k < K) {
-            v = src[r * ld + k];
-            if (mask != nullptr && !(mask[r * ld + k] > 0.0f)) v = 0.0f;
+        const int64_t r = e / groups, k0 = (e - r * groups) * 8;
+        const float* sr = src + r * ld + k0;
+        const float* mr = mask != nullptr ? mask + r * ld + k0 : nullptr;
+        float v[8];
+        if (vec && k0 + 8 <= K) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(sr)), b = __ldg(reinterpret_cast<const float4*>(sr) + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            if (mr != nullptr) {
+                const float4 c = __ldg(reinterpret_cast<const float4*>(mr)), d = __ldg(reinterpret_cast<const float4*>(mr) + 1);
+                const float m[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (!(m[i] > 0.0f)) v[i] = 0.0f;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[i] = k0 + i < K ? __ldg(sr + i) : 0.0f;
+                if (mr != nullptr && k0 + i < K && !(__ldg(mr + i) > 0.0f)) v[i] = 0.0f;
+            }
         }
-        split_one(v, hi[e], lo[e]);
+        uint4 h, l;
+        split8(v, h, l);
+        reinterpret_cast<uint4*>(hi + r * Kp + k0)[0] = h;
+        reinterpret_cast<uint4*>(lo + r * Kp + k0)[0] = l;
     }
 }
 
-// hi / lo [C x Rp] of the transpose of src [R x C] (times [mask > 0]); columns R .. Rp - 1 are zero.
-// 32 x 32 tiles through shared memory.
+// hi / lo [C x Rp] of the transpose of src [R x C] (times [mask > 0]); columns R .. Rp - 1 are zero (Rp is
+// even).  Tiles of 64 rows x 32 columns through shared memory; a thread writes two consecutive rows of a
+// column as one bf16 pair, so a warp stores 128 contiguous bytes.
 __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src,
                                                               const float* __restrict__ mask, int64_t R, int64_t C,
                                                               int64_t Rp, __nv_bfloat16* __restrict__ hi,
                                                               __nv_bfloat16* __restrict__ lo)
 {
-    __shared__ float tile[32][33];
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 32;
+    __shared__ float tile[64][33];
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 64;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int j = ty; j < 32; j += 8) {
+    for (int j = ty; j < 64; j += 8) {
         const int64_t r = r0 + j, c = c0 + tx;
         float v = 0.0f;
         if (r < R && c < C) {
@@ -229,9 +269,21 @@ __global__ void __launch_bounds__(256) split_transpose_kernel(const float* __res
         tile[j][tx] = v;
     }
     __syncthreads();
-    for (int j = ty; j < 32; j += 8) {
-        const int64_t c = c0 + j, r = r0 + tx;
-        if (c < C && r < Rp) split_one(r < R ? tile[tx][j] : 0.0f, hi[c * Rp + r], lo[c * Rp + r]);
+    const int64_t r = r0 + 2 * tx;
+    if (r < Rp) {
+        for (int j = ty; j < 32; j += 8) {
+            const int64_t c = c0 + j;
+            if (c < C) {
+                __nv_bfloat16 h0, l0, h1, l1;
+                split_one(tile[2 * tx][j], h0, l0);  // rows past R hold zero
+                split_one(tile[2 * tx + 1][j], h1, l1);
+                __nv_bfloat162 hp, lp;
+                hp.x = h0; hp.y = h1;
+                lp.x = l0; lp.y = l1;
+                *reinterpret_cast<__nv_bfloat162*>(hi + c * Rp + r) = hp;
+                *reinterpret_cast<__nv_bfloat162*>(lo + c * Rp + r) = lp;
+            }
+        }
     }
 }
 
@@ -473,16 +525,18 @@ struct Carver {
 void split_rows(const float* src, const float* mask, int64_t ld, int64_t R, int64_t K, int64_t Kp, __nv_bfloat16* hi,
                 __nv_bfloat16* lo, cudaStream_t s)
 {
-    const int64_t n = R * Kp;
+    const int64_t n = R * (Kp / 8);
     const int64_t blocks = (n + 255) / 256;
+    const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const int vec = ld % 4 == 0 && a16(src) && (mask == nullptr || a16(mask));
     split_rows_kernel<<<static_cast<unsigned>(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, s>>>(src, mask, ld, R, K,
-                                                                                                   Kp, hi, lo);
+                                                                                                   Kp, vec, hi, lo);
 }
 
 void split_transpose(const float* src, const float* mask, int64_t R, int64_t C, int64_t Rp, __nv_bfloat16* hi,
                      __nv_bfloat16* lo, cudaStream_t s)
 {
-    const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((Rp + 31) / 32));
+    const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((Rp + 63) / 64));
     split_transpose_kernel<<<grid, 256, 0, s>>>(src, mask, R, C, Rp, hi, lo);
 }
 
