@@ -19,12 +19,12 @@
 // store through a transpose in shared memory so that stores are row-contiguous.
 //
 // Backward of y = act(x W^T + b) from dy: dz = dy * [y > 0] (ReLU) or dy;
-// dx = dz W; dW = dz^T x; db = sum over the batch of dz.  dx is a GEMM with A =
-// dz (the mask applied while dz is split) and B = W^T (an explicit transpose of
-// the small W); dW is a GEMM over the batch with A = dz^T and B = x^T (tiled
-// transposes through shared memory, the mask applied in the transpose), split
-// over the batch into partial sums that the update kernel adds in a fixed order
-// (bitwise reproducible) before W -= lr dW, b -= lr db.
+// dx = dz W; dW = dz^T x; db = sum over the batch of dz.  dz (the mask applied
+// while it is split), x and W are each split once, row by row; the transposed
+// operands (W in dx, dz and x in dW) are the same arrays read MN-major by the
+// tensor cores, so nothing is transposed in memory.  dW is split over the batch
+// into partial sums that the update kernel adds in a fixed order (bitwise
+// reproducible) before W -= lr dW, b -= lr db.
 //
 // Head.  The last top layer maps to one logit: a warp per sample computes
 // z = h . w + b, p = sigmoid(z), the sample's BCE term max(z, 0) - z y +
@@ -53,8 +53,12 @@ constexpr int kStage = 4 * kTile;           // A hi, A lo, B hi, B lo: 64 KB
 constexpr int kGemmSmem = kStages * kStage + 1024 + 128;
 constexpr uint32_t kFull = 0xffffffffu;
 
+// An operand is K-major (bf16 [rows x Kp] with the K values of a row contiguous; box 64 K x 128 rows) or
+// MN-major (bf16 [K x MNp] with the M (or N) values of one k contiguous; box 64 M x 64 K, two boxes per
+// 128-wide tile).  Both land as 16 KB per operand and stage in the 128-byte swizzle layout.
 struct GemmArgs {
-    CUtensorMap a_hi, a_lo, b_hi, b_lo;  // bf16 [rows x Kp], box 64 x 128, 128-byte swizzle
+    CUtensorMap a_hi, a_lo, b_hi, b_lo;
+    int a_mn, b_mn;                      // MN-major A / B
     const float* bias;                   // optional, N values
     float* c;
     int64_t ldc;
@@ -73,6 +77,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
         : "memory");
 }
+
+// Shared-memory matrix descriptor of an MN-major bf16 operand in the 128-byte swizzle layout: a 128-B row
+// holds 64 consecutive M (or N) values of one k, consecutive k are consecutive rows, 8-row groups 1024 B
+// apart (stride byte offset), the next 64 M (or N) values kMnBlock bytes later (leading byte offset).
+// Moving the start by 2048 B selects the next 16 of K.
+constexpr uint32_t kMnBlock = kBK * 128;  // one 64 x 64 box: 8 KB
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)  // start address
+           | (static_cast<uint64_t>(kMnBlock >> 4) << 16)   // leading byte offset: next 64 of M (or N)
+           | (static_cast<uint64_t>(1024 >> 4) << 32)       // stride byte offset: next 8 rows of K
+           | (static_cast<uint64_t>(1) << 46)               // descriptor version of tcgen05
+           | (static_cast<uint64_t>(2) << 61);              // 128-byte swizzle
+}
+
+// Transpose bits of the kind::f16 instruction descriptor: A (bit 15), B (bit 16) MN-major.
+constexpr uint32_t kIdescAMn = 1u << 15, kIdescBMn = 1u << 16;
 
 __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs g)
 {
@@ -114,15 +135,25 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
             if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1);
             if (!ok) break;
             mbar_arrive_expect_tx(&full[s], kStage);
-            const int x = static_cast<int>(kb + static_cast<int64_t>(i) * kBK);
-            tma_load_2d(tile(s, 0), &g.a_hi, x, static_cast<int>(m0), &full[s]);
-            tma_load_2d(tile(s, 1), &g.a_lo, x, static_cast<int>(m0), &full[s]);
-            tma_load_2d(tile(s, 2), &g.b_hi, x, static_cast<int>(n0), &full[s]);
-            tma_load_2d(tile(s, 3), &g.b_lo, x, static_cast<int>(n0), &full[s]);
+            const int k = static_cast<int>(kb + static_cast<int64_t>(i) * kBK);
+            auto load = [&](int which, const CUtensorMap* map, int mn_major, int64_t row0) {
+                if (mn_major) {  // two 64 x 64 boxes: M (or N) values row0 .. +63, then +64 .. +127
+                    tma_load_2d(tile(s, which), map, static_cast<int>(row0), k, &full[s]);
+                    tma_load_2d(tile(s, which) + kMnBlock, map, static_cast<int>(row0) + 64, k, &full[s]);
+                } else {
+                    tma_load_2d(tile(s, which), map, k, static_cast<int>(row0), &full[s]);
+                }
+            };
+            load(0, &g.a_hi, g.a_mn, m0);
+            load(1, &g.a_lo, g.a_mn, m0);
+            load(2, &g.b_hi, g.b_mn, n0);
+            load(3, &g.b_lo, g.b_mn, n0);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer: hi*hi, hi*lo, lo*hi over 4 steps of K = 16 per slice; each slice's stage released on commit
-        constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+        const uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN) | (g.a_mn ? kIdescAMn : 0u) | (g.b_mn ? kIdescBMn : 0u);
+        // the next 16 of K: 32 B along a K-major row, 2048 B (16 rows) down an MN-major tile
+        const uint32_t a_step = g.a_mn ? 2048u : 32u, b_step = g.b_mn ? 2048u : 32u;
         for (int i = 0; i < nk && ok; ++i) {
             const int s = i % kStages;
             ok = mbar_wait_bounded(&full[s], (i / kStages) & 1);
@@ -133,9 +164,11 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
 #pragma unroll
             for (int it = 0; it < 12; ++it) {
                 const int pass = it / 4, ks = it % 4;
-                const uint32_t A = (pass == 2 ? al : ah) + ks * 32;
-                const uint32_t B = (pass == 1 ? bl : bh) + ks * 32;
-                tc::mma_bf16(tmem, tc::desc_kmajor_sw128(A), tc::desc_kmajor_sw128(B), idesc, (i > 0 || it > 0) ? 1u : 0u);
+                const uint32_t A = (pass == 2 ? al : ah) + ks * a_step;
+                const uint32_t B = (pass == 1 ? bl : bh) + ks * b_step;
+                const uint64_t da = g.a_mn ? desc_mnmajor_sw128(A) : tc::desc_kmajor_sw128(A);
+                const uint64_t db = g.b_mn ? desc_mnmajor_sw128(B) : tc::desc_kmajor_sw128(B);
+                tc::mma_bf16(tmem, da, db, idesc, (i > 0 || it > 0) ? 1u : 0u);
             }
             tc::commit(&empty[s]);
         }
@@ -245,45 +278,6 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
         split8(v, h, l);
         reinterpret_cast<uint4*>(hi + r * Kp + k0)[0] = h;
         reinterpret_cast<uint4*>(lo + r * Kp + k0)[0] = l;
-    }
-}
-
-// hi / lo [C x Rp] of the transpose of src [R x C] (times [mask > 0]); columns R .. Rp - 1 are zero (Rp is
-// even).  Tiles of 64 rows x 32 columns through shared memory; a thread writes two consecutive rows of a
-// column as one bf16 pair, so a warp stores 128 contiguous bytes.
-__global__ void __launch_bounds__(256) split_transpose_kernel(const float* __restrict__ src,
-                                                              const float* __restrict__ mask, int64_t R, int64_t C,
-                                                              int64_t Rp, __nv_bfloat16* __restrict__ hi,
-                                                              __nv_bfloat16* __restrict__ lo)
-{
-    __shared__ float tile[64][33];
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32, r0 = static_cast<int64_t>(blockIdx.y) * 64;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    for (int j = ty; j < 64; j += 8) {
-        const int64_t r = r0 + j, c = c0 + tx;
-        float v = 0.0f;
-        if (r < R && c < C) {
-            v = src[r * C + c];
-            if (mask != nullptr && !(mask[r * C + c] > 0.0f)) v = 0.0f;
-        }
-        tile[j][tx] = v;
-    }
-    __syncthreads();
-    const int64_t r = r0 + 2 * tx;
-    if (r < Rp) {
-        for (int j = ty; j < 32; j += 8) {
-            const int64_t c = c0 + j;
-            if (c < C) {
-                __nv_bfloat16 h0, l0, h1, l1;
-                split_one(tile[2 * tx][j], h0, l0);  // rows past R hold zero
-                split_one(tile[2 * tx + 1][j], h1, l1);
-                __nv_bfloat162 hp, lp;
-                hp.x = h0; hp.y = h1;
-                lp.x = l0; lp.y = l1;
-                *reinterpret_cast<__nv_bfloat162*>(hi + c * Rp + r) = hp;
-                *reinterpret_cast<__nv_bfloat162*>(lo + c * Rp + r) = lp;
-            }
-        }
     }
 }
 
@@ -463,33 +457,44 @@ EncodeFn encoder()
     return reinterpret_cast<EncodeFn>(f);
 }
 
-// A bf16 [rows x kp] row-major operand, tiles of 64 (K) x 128 rows, 128-byte swizzle, zero fill out of range.
-bool encode_operand(CUtensorMap* map, const __nv_bfloat16* base, int64_t rows, int64_t kp)
+// A split operand in global memory: bf16 hi / lo [outer x inner] row-major (inner a multiple of 8).  K-major:
+// outer = M (or N) rows of K values; MN-major: outer = K rows of M (or N) values.
+struct Operand {
+    const __nv_bfloat16 *hi, *lo;
+    int64_t inner, outer;
+    int mn;
+};
+
+// Tiles of 64 inner x (128 rows K-major, 64 rows MN-major), 128-byte swizzle, zero fill out of range.
+bool encode_operand(CUtensorMap* map, const __nv_bfloat16* base, const Operand& op)
 {
     EncodeFn enc = encoder();
     if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kp) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.inner), static_cast<cuuint64_t>(op.outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.inner) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(op.mn ? kBK : kBM)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// C = A B^T from split operands: A hi / lo [M x kp], B hi / lo [N x kp], K the reduction length (<= kp).
-dlrm_status launch_gemm(const __nv_bfloat16* ah, const __nv_bfloat16* al, const __nv_bfloat16* bh,
-                        const __nv_bfloat16* bl, int64_t kp, const float* bias, float* c, int64_t ldc, int64_t M,
+// C[M x N] = A B^T (A: M x K, B: N x K, each K-major or MN-major), K the reduction length; splits > 1: split-K
+// partials split_stride elements apart.
+dlrm_status launch_gemm(const Operand& A, const Operand& B, const float* bias, float* c, int64_t ldc, int64_t M,
                         int64_t N, int64_t K, int relu, int splits, int64_t split_stride, int32_t* status,
                         cudaStream_t s)
 {
     if (M <= 0 || N <= 0) return DLRM_OK;
-    if (M > INT32_MAX || N > INT32_MAX || kp > INT32_MAX) return DLRM_ERR_UNSUPPORTED;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || A.inner > INT32_MAX || B.inner > INT32_MAX)
+        return DLRM_ERR_UNSUPPORTED;
     GemmArgs g;
     memset(&g, 0, sizeof g);
-    if (!encode_operand(&g.a_hi, ah, M, kp) || !encode_operand(&g.a_lo, al, M, kp) ||
-        !encode_operand(&g.b_hi, bh, N, kp) || !encode_operand(&g.b_lo, bl, N, kp))
+    if (!encode_operand(&g.a_hi, A.hi, A) || !encode_operand(&g.a_lo, A.lo, A) || !encode_operand(&g.b_hi, B.hi, B) ||
+        !encode_operand(&g.b_lo, B.lo, B))
         return DLRM_ERR_CUDA;
+    g.a_mn = A.mn;
+    g.b_mn = B.mn;
     g.bias = bias;
     g.c = c;
     g.ldc = ldc;
@@ -533,13 +538,6 @@ void split_rows(const float* src, const float* mask, int64_t ld, int64_t R, int6
                                                                                                    Kp, vec, hi, lo);
 }
 
-void split_transpose(const float* src, const float* mask, int64_t R, int64_t C, int64_t Rp, __nv_bfloat16* hi,
-                     __nv_bfloat16* lo, cudaStream_t s)
-{
-    const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((Rp + 63) / 64));
-    split_transpose_kernel<<<grid, 256, 0, s>>>(src, mask, R, C, Rp, hi, lo);
-}
-
 // Workspace of the forward: x and W split.
 struct FwdWs {
     __nv_bfloat16 *xh, *xl, *wh, *wl;
@@ -557,27 +555,26 @@ FwdWs carve_fwd(void* base, int64_t M, int32_t K, int32_t N, size_t* bytes)
     return w;
 }
 
-// Workspace of the backward: dz and W^T split (dx), dz^T and x^T split (dW), the dW partials, the db partials.
+// Workspace of the backward: dz, W and x split once (row by row); dx and dW read them K-major or MN-major as
+// each product needs; the dW partials, the db partials.
 struct BwdWs {
-    __nv_bfloat16 *dzh, *dzl, *wth, *wtl, *dzth, *dztl, *xth, *xtl;
+    __nv_bfloat16 *dzh, *dzl, *wh, *wl, *xh, *xl;
     float *part, *db_part;
     int splits;
 };
 BwdWs carve_bwd(void* base, int64_t M, int32_t K, int32_t N, size_t* bytes)
 {
     Carver c{static_cast<char*>(base)};
-    const int64_t np = pad8(N), mp = pad8(M);
+    const int64_t np = pad8(N), kp = pad8(K);
     BwdWs w;
     const int64_t tiles = ((N + kBM - 1) / kBM) * ((K + kBN - 1) / kBN);
     w.splits = splits_for(tiles, M);
     w.dzh = c.take<__nv_bfloat16>(M * np);
     w.dzl = c.take<__nv_bfloat16>(M * np);
-    w.wth = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * np);
-    w.wtl = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * np);
-    w.dzth = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * mp);
-    w.dztl = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * mp);
-    w.xth = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * mp);
-    w.xtl = c.take<__nv_bfloat16>(static_cast<int64_t>(K) * mp);
+    w.wh = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * kp);
+    w.wl = c.take<__nv_bfloat16>(static_cast<int64_t>(N) * kp);
+    w.xh = c.take<__nv_bfloat16>(M * kp);
+    w.xl = c.take<__nv_bfloat16>(M * kp);
     w.part = c.take<float>(static_cast<size_t>(w.splits) * N * K);
     w.db_part = c.take<float>(static_cast<size_t>(kColChunks) * N);
     if (bytes) *bytes = c.used;
@@ -607,7 +604,9 @@ dlrm_status launch_fc_fwd(const float* x, const float* w, const float* b, int64_
     const int64_t kp = pad8(K);
     split_rows(x, nullptr, K, M, K, kp, ws.xh, ws.xl, s);
     split_rows(w, nullptr, K, N, K, kp, ws.wh, ws.wl, s);
-    return launch_gemm(ws.xh, ws.xl, ws.wh, ws.wl, kp, b, y, N, M, N, K, relu, 1, 0, status, s);
+    // y = x W^T: A = x [M x K], B = W [N x K], both K-major
+    const Operand A{ws.xh, ws.xl, kp, M, 0}, B{ws.wh, ws.wl, kp, N, 0};
+    return launch_gemm(A, B, b, y, N, M, N, K, relu, 1, 0, status, s);
 }
 
 dlrm_status launch_fc_bwd_sgd(const float* x, float* w, float* b, const float* y, const float* dy, int64_t M, int32_t K,
@@ -615,20 +614,20 @@ dlrm_status launch_fc_bwd_sgd(const float* x, float* w, float* b, const float* y
                               cudaStream_t s)
 {
     const BwdWs ws = carve_bwd(workspace, M, K, N, nullptr);
-    const int64_t np = pad8(N), mp = pad8(M);
+    const int64_t np = pad8(N), kp = pad8(K);
     const float* mask = relu ? y : nullptr;
-    // dx = dz W: A = dz [M x N] (mask applied), B = W^T [K x N]
+    split_rows(dy, mask, N, M, N, np, ws.dzh, ws.dzl, s);  // dz = dy [y > 0], [M x N]
+    split_rows(x, nullptr, K, M, K, kp, ws.xh, ws.xl, s);  // x [M x K]
+    // dx = dz W: A = dz [M x N] K-major; B[k][n] = W[n][k]: W [N x K] read MN-major
     if (dx != nullptr) {
-        split_rows(dy, mask, N, M, N, np, ws.dzh, ws.dzl, s);
-        split_transpose(w, nullptr, N, K, np, ws.wth, ws.wtl, s);
-        dlrm_status st = launch_gemm(ws.dzh, ws.dzl, ws.wth, ws.wtl, np, nullptr, dx, K, M, K, N, 0, 1, 0, status, s);
+        split_rows(w, nullptr, K, N, K, kp, ws.wh, ws.wl, s);
+        const Operand A{ws.dzh, ws.dzl, np, M, 0}, B{ws.wh, ws.wl, kp, N, 1};
+        dlrm_status st = launch_gemm(A, B, nullptr, dx, K, M, K, N, 0, 1, 0, status, s);
         if (st != DLRM_OK) return st;
     }
-    // dW = dz^T x over the batch, in split partials: A = dz^T [N x M], B = x^T [K x M]
-    split_transpose(dy, mask, M, N, mp, ws.dzth, ws.dztl, s);
-    split_transpose(x, nullptr, M, K, mp, ws.xth, ws.xtl, s);
-    dlrm_status st = launch_gemm(ws.dzth, ws.dztl, ws.xth, ws.xtl, mp, nullptr, ws.part, K, N, K, M, 0, ws.splits,
-                                 static_cast<int64_t>(N) * K, status, s);
+    // dW = dz^T x over the batch, in split partials: A[n][m] = dz[m][n], B[k][m] = x[m][k], both read MN-major
+    const Operand A{ws.dzh, ws.dzl, np, M, 1}, B{ws.xh, ws.xl, kp, M, 1};
+    dlrm_status st = launch_gemm(A, B, nullptr, ws.part, K, N, K, M, 0, ws.splits, static_cast<int64_t>(N) * K, status, s);
     if (st != DLRM_OK) return st;
     if (b != nullptr) {
         const dim3 grid(static_cast<unsigned>((N + 31) / 32), kColChunks);
