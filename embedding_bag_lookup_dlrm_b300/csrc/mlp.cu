@@ -45,12 +45,14 @@
 namespace dlrm {
 namespace {
 
-constexpr int kGThreads = 128;  // warp 0: TMA producer, warp 1: MMA issuer; all four: epilogue
+constexpr int kEpiWarps = 4;                    // warps 2-5: the epilogue, one per quarter of the TMEM lanes
+constexpr int kGThreads = (2 + kEpiWarps) * 32;  // warp 0: TMA producer, warp 1: MMA issuer
 constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr int kStages = 3;
 constexpr int kTile = kBM * kBK * 2;        // one bf16 operand tile, 16 KB (kBM == kBN)
 constexpr int kStage = 4 * kTile;           // A hi, A lo, B hi, B lo: 64 KB
-constexpr int kGemmSmem = kStages * kStage + 1024 + 128;
+constexpr int kEpiBytes = kEpiWarps * 32 * 33 * 4;  // the epilogue's transposes
+constexpr int kGemmSmem = kStages * kStage + 1024 + 128 + kEpiBytes;
 constexpr uint32_t kFull = 0xffffffffu;
 
 // An operand is K-major (bf16 [rows x Kp] with the K values of a row contiguous; box 64 K x 128 rows) or
@@ -63,6 +65,7 @@ struct GemmArgs {
     float* c;
     int64_t ldc;
     int64_t M, N, K;
+    int64_t splits;        // split-K: tiles z = 0 .. splits - 1 of each output tile
     int64_t k_per_split;   // reduction range of split z: [z * k_per_split, min(K, (z + 1) * k_per_split))
     int64_t split_stride;  // elements between the C partials of consecutive splits
     int relu;
@@ -95,30 +98,39 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr)
 // Transpose bits of the kind::f16 instruction descriptor: A (bit 15), B (bit 16) MN-major.
 constexpr uint32_t kIdescAMn = 1u << 15, kIdescBMn = 1u << 16;
 
+// One CTA per SM walks tiles blockIdx.x, + gridDim.x, ... (M fastest, so CTAs running at once share B
+// tiles in L2).  Warp 0 (one thread) loads slices into the ring, warp 1 (one thread) issues the MMAs of a
+// tile into one of two TMEM accumulators, warps 2-5 drain the other accumulator: tile i's epilogue runs
+// beside tile i + 1's MMAs.
 __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs g)
 {
     extern __shared__ unsigned char gsm_raw[];
     unsigned char* sm = gsm_raw + ((1024u - (smem_addr(gsm_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + kStages * kStage);
     uint64_t* empty = full + kStages;
-    uint64_t* done = empty + kStages;
+    uint64_t* acc_full = empty + kStages;  // [2] the MMAs of the accumulator's tile completed
+    uint64_t* acc_empty = acc_full + 2;    // [2] the epilogue has read the accumulator out
+    uint64_t* done = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    float* epi = reinterpret_cast<float*>(sm + kStages * kStage + 128);  // 4 x 32 x 33 floats
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kBM, n0 = static_cast<int64_t>(blockIdx.y) * kBN;
-    const int64_t kb = static_cast<int64_t>(blockIdx.z) * g.k_per_split;
-    const int64_t ke = min(g.K, kb + g.k_per_split);
-    const int nk = ke > kb ? static_cast<int>((ke - kb + kBK - 1) / kBK) : 0;
+    const int64_t mt = (g.M + kBM - 1) / kBM, nt = (g.N + kBN - 1) / kBN;
+    const int64_t tiles = mt * nt * g.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], kEpiWarps);
+        }
         mbar_init(done, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, kBN);
+        tc::tmem_alloc(tmem_slot, 2 * kBN);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -126,97 +138,138 @@ __global__ void __launch_bounds__(kGThreads, 1) gemm_tc_kernel(const __grid_cons
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     auto tile = [&](int s, int which) { return sm + s * kStage + which * kTile; };
+    // tile t: rows m0, columns n0, reduction range [kb, ke) in nk slices
+    struct Tile {
+        int64_t m0, n0, z, kb;
+        int nk;
+    };
+    auto tile_of = [&](int64_t t) {
+        Tile r;
+        r.z = t / (mt * nt);
+        const int64_t rem = t - r.z * mt * nt;
+        r.m0 = (rem % mt) * kBM;
+        r.n0 = (rem / mt) * kBN;
+        r.kb = r.z * g.k_per_split;
+        const int64_t ke = min(g.K, r.kb + g.k_per_split);
+        r.nk = ke > r.kb ? static_cast<int>((ke - r.kb + kBK - 1) / kBK) : 0;
+        return r;
+    };
 
     bool ok = true;
     if (warp == 0 && lane == 0) {
-        // producer: stage s of slice i, once the MMAs of slice i - kStages have read it
-        for (int i = 0; i < nk && ok; ++i) {
-            const int s = i % kStages;
-            if (i >= kStages) ok = mbar_wait_bounded(&empty[s], ((i / kStages) - 1) & 1);
-            if (!ok) break;
-            mbar_arrive_expect_tx(&full[s], kStage);
-            const int k = static_cast<int>(kb + static_cast<int64_t>(i) * kBK);
-            auto load = [&](int which, const CUtensorMap* map, int mn_major, int64_t row0) {
-                if (mn_major) {  // two 64 x 64 boxes: M (or N) values row0 .. +63, then +64 .. +127
-                    tma_load_2d(tile(s, which), map, static_cast<int>(row0), k, &full[s]);
-                    tma_load_2d(tile(s, which) + kMnBlock, map, static_cast<int>(row0) + 64, k, &full[s]);
-                } else {
-                    tma_load_2d(tile(s, which), map, k, static_cast<int>(row0), &full[s]);
-                }
-            };
-            load(0, &g.a_hi, g.a_mn, m0);
-            load(1, &g.a_lo, g.a_mn, m0);
-            load(2, &g.b_hi, g.b_mn, n0);
-            load(3, &g.b_lo, g.b_mn, n0);
+        // producer: the q-th slice of this CTA goes to stage q % kStages once the MMAs of slice q - kStages
+        // have read it
+        uint32_t q = 0;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            const Tile tl = tile_of(t);
+            for (int i = 0; i < tl.nk && ok; ++i, ++q) {
+                const int s = static_cast<int>(q % kStages);
+                if (q >= kStages) ok = mbar_wait_bounded(&empty[s], ((q / kStages) - 1) & 1);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&full[s], kStage);
+                const int k = static_cast<int>(tl.kb + static_cast<int64_t>(i) * kBK);
+                auto load = [&](int which, const CUtensorMap* map, int mn_major, int64_t row0) {
+                    if (mn_major) {  // two 64 x 64 boxes: M (or N) values row0 .. +63, then +64 .. +127
+                        tma_load_2d(tile(s, which), map, static_cast<int>(row0), k, &full[s]);
+                        tma_load_2d(tile(s, which) + kMnBlock, map, static_cast<int>(row0) + 64, k, &full[s]);
+                    } else {
+                        tma_load_2d(tile(s, which), map, k, static_cast<int>(row0), &full[s]);
+                    }
+                };
+                load(0, &g.a_hi, g.a_mn, tl.m0);
+                load(1, &g.a_lo, g.a_mn, tl.m0);
+                load(2, &g.b_hi, g.b_mn, tl.n0);
+                load(3, &g.b_lo, g.b_mn, tl.n0);
+            }
         }
     } else if (warp == 1 && lane == 0) {
-        // MMA issuer: hi*hi, hi*lo, lo*hi over 4 steps of K = 16 per slice; each slice's stage released on commit
+        // MMA issuer: per slice hi*hi, hi*lo, lo*hi over 4 steps of K = 16, the stage released on commit;
+        // per tile the accumulator j % 2, once the epilogue has drained it (tile j - 2)
         const uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN) | (g.a_mn ? kIdescAMn : 0u) | (g.b_mn ? kIdescBMn : 0u);
         // the next 16 of K: 32 B along a K-major row, 2048 B (16 rows) down an MN-major tile
         const uint32_t a_step = g.a_mn ? 2048u : 32u, b_step = g.b_mn ? 2048u : 32u;
-        for (int i = 0; i < nk && ok; ++i) {
-            const int s = i % kStages;
-            ok = mbar_wait_bounded(&full[s], (i / kStages) & 1);
+        uint32_t q = 0, j = 0;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++j) {
+            const Tile tl = tile_of(t);
+            const uint32_t acc = j & 1u;
+            if (j >= 2) ok = mbar_wait_bounded(&acc_empty[acc], ((j / 2) - 1) & 1);
             if (!ok) break;
             tc::fence_after_sync();
-            const uint32_t ah = smem_addr(tile(s, 0)), al = smem_addr(tile(s, 1));
-            const uint32_t bh = smem_addr(tile(s, 2)), bl = smem_addr(tile(s, 3));
+            const uint32_t d = tmem + acc * kBN;
+            for (int i = 0; i < tl.nk && ok; ++i, ++q) {
+                const int s = static_cast<int>(q % kStages);
+                ok = mbar_wait_bounded(&full[s], (q / kStages) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t ah = smem_addr(tile(s, 0)), al = smem_addr(tile(s, 1));
+                const uint32_t bh = smem_addr(tile(s, 2)), bl = smem_addr(tile(s, 3));
 #pragma unroll
-            for (int it = 0; it < 12; ++it) {
-                const int pass = it / 4, ks = it % 4;
-                const uint32_t A = (pass == 2 ? al : ah) + ks * a_step;
-                const uint32_t B = (pass == 1 ? bl : bh) + ks * b_step;
-                const uint64_t da = g.a_mn ? desc_mnmajor_sw128(A) : tc::desc_kmajor_sw128(A);
-                const uint64_t db = g.b_mn ? desc_mnmajor_sw128(B) : tc::desc_kmajor_sw128(B);
-                tc::mma_bf16(tmem, da, db, idesc, (i > 0 || it > 0) ? 1u : 0u);
+                for (int it = 0; it < 12; ++it) {
+                    const int pass = it / 4, ks = it % 4;
+                    const uint32_t A = (pass == 2 ? al : ah) + ks * a_step;
+                    const uint32_t B = (pass == 1 ? bl : bh) + ks * b_step;
+                    const uint64_t da = g.a_mn ? desc_mnmajor_sw128(A) : tc::desc_kmajor_sw128(A);
+                    const uint64_t db = g.b_mn ? desc_mnmajor_sw128(B) : tc::desc_kmajor_sw128(B);
+                    tc::mma_bf16(d, da, db, idesc, (i > 0 || it > 0) ? 1u : 0u);
+                }
+                tc::commit(&empty[s]);
             }
-            tc::commit(&empty[s]);
+            tc::commit(&acc_full[acc]);  // arrives once every MMA issued above has completed
         }
-        tc::commit(done);  // every MMA issued above has completed when this arrives
+        tc::commit(done);
+    } else if (warp >= 2) {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (rows of the tile), 32 columns at a time, adds
+        // the bias and applies ReLU (or writes a split-K partial), and passes them through a 32 x 33
+        // transpose in shared memory so that each store instruction writes 32 consecutive columns of a row
+        const int quarter = warp % 4;
+        float* stage = epi + (warp - 2) * (32 * 33);
+        uint32_t j = 0;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++j) {
+            const Tile tl = tile_of(t);
+            const uint32_t acc = j & 1u;
+            ok = mbar_wait_bounded(&acc_full[acc], (j / 2) & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            float* cbase = g.c + tl.z * g.split_stride;
+            const int64_t mw = tl.m0 + 32 * quarter;
+            const int rows = static_cast<int>(min(static_cast<int64_t>(32), g.M - mw));
+#pragma unroll 1
+            for (int cb = 0; cb < kBN / 32; ++cb) {
+                uint32_t r[32];
+                tc::tmem_ld_32x32b_x32(tmem + acc * kBN + ((static_cast<uint32_t>(32 * quarter)) << 16) +
+                                           static_cast<uint32_t>(32 * cb),
+                                       r);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c)  // an empty reduction range contributes zero
+                    stage[lane * 33 + c] = tl.nk == 0 ? 0.0f : __uint_as_float(r[c]);
+                __syncwarp();
+                const int64_t n = tl.n0 + 32 * cb + lane;
+                const bool col = n < g.N;
+                const float bias = (col && g.bias != nullptr) ? __ldg(g.bias + n) : 0.0f;
+                for (int i = 0; i < rows; ++i) {
+                    if (col) {
+                        float v = stage[i * 33 + lane];
+                        if (g.bias != nullptr) v += bias;
+                        if (g.relu) v = fmaxf(v, 0.0f);
+                        cbase[(mw + i) * g.ldc + n] = v;
+                    }
+                }
+                __syncwarp();  // the stage is rewritten by the next column block
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);  // the accumulator may take tile j + 2
+        }
     }
     __syncwarp();
-    if (nk > 0) ok &= mbar_wait_bounded(done, 0);
+    tc::fence_before_sync();
+    ok = mbar_wait_bounded(done, 0) && ok;  // every MMA of this CTA has completed
     ok = __syncthreads_and(ok) != 0;
     if (!ok && threadIdx.x == 0) flag_status(g.status, DLRM_ERR_TIMEOUT);
-    tc::fence_after_sync();
-
-    // epilogue: warp w reads rows 32 w + lane of the accumulator, 32 columns at a time, and passes them
-    // through a 32 x 33 transpose in the (now idle) operand ring, so that each store instruction writes 32
-    // consecutive columns of one row of C
-    if (ok) {
-        tc::fence_smem_for_mma();  // the ring was last read by the MMAs (async proxy)
-        float* stage = reinterpret_cast<float*>(sm) + warp * (32 * 33);
-        float* cbase = g.c + static_cast<int64_t>(blockIdx.z) * g.split_stride;
-        const int64_t mw = m0 + 32 * warp;
-#pragma unroll 1
-        for (int cb = 0; cb < kBN / 32; ++cb) {
-            uint32_t r[32];
-            tc::tmem_ld_32x32b_x32(tmem + ((static_cast<uint32_t>(32 * warp)) << 16) + static_cast<uint32_t>(32 * cb), r);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j)  // an empty reduction range contributes zero
-                stage[lane * 33 + j] = nk == 0 ? 0.0f : __uint_as_float(r[j]);
-            __syncwarp();
-            const int64_t n = n0 + 32 * cb + lane;
-            const bool col = n < g.N;
-            const float bias = (col && g.bias != nullptr) ? __ldg(g.bias + n) : 0.0f;
-            const int rows = static_cast<int>(min(static_cast<int64_t>(32), g.M - mw));
-            for (int i = 0; i < rows; ++i) {
-                if (col) {
-                    float v = stage[i * 33 + lane];
-                    if (g.bias != nullptr) v += bias;
-                    if (g.relu) v = fmaxf(v, 0.0f);
-                    cbase[(mw + i) * g.ldc + n] = v;
-                }
-            }
-            __syncwarp();  // the stage is rewritten by the next column block
-        }
-    }
-    tc::fence_before_sync();
-    __syncthreads();
     if (warp == 0) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kBN);
+        tc::tmem_dealloc(tmem, 2 * kBN);
     }
 }
 
@@ -281,8 +334,9 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
     }
 }
 
-// Column sums of src [R x C] (times [mask > 0]) over row chunks: part[chunk][c]; a fixed order.
-constexpr int kColChunks = 64;
+// Column sums of src [R x C] (times [mask > 0]) over row chunks: part[chunk][c]; a fixed order.  Enough
+// chunks that the batch's columns keep every SM busy (4,096 blocks for C = 512).
+constexpr int kColChunks = 256;
 __global__ void __launch_bounds__(256) col_sum_kernel(const float* __restrict__ src, const float* __restrict__ mask,
                                                       int64_t R, int64_t C, float* __restrict__ part)
 {
@@ -293,6 +347,7 @@ __global__ void __launch_bounds__(256) col_sum_kernel(const float* __restrict__ 
     const int64_t r_lo = static_cast<int64_t>(blockIdx.y) * per, r_hi = min(R, r_lo + per);
     float s = 0.0f;
     if (c < C)
+#pragma unroll 4
         for (int64_t r = r_lo + ty; r < r_hi; r += 8) {
             float v = src[r * C + c];
             if (mask != nullptr && !(mask[r * C + c] > 0.0f)) v = 0.0f;
@@ -503,13 +558,16 @@ dlrm_status launch_gemm(const Operand& A, const Operand& B, const float* bias, f
     g.K = K;
     const int64_t per = (K + splits - 1) / splits;
     g.k_per_split = (per + kBK - 1) / kBK * kBK;
+    g.splits = splits;
     g.split_stride = split_stride;
     g.relu = relu;
     g.status = status;
     if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) != cudaSuccess)
         return DLRM_ERR_CUDA;
-    const dim3 grid(static_cast<unsigned>((M + kBM - 1) / kBM), static_cast<unsigned>((N + kBN - 1) / kBN),
-                    static_cast<unsigned>(splits));
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN) * splits;
+    const int sms = sm_count();
+    if (sms <= 0) return DLRM_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);  // one CTA per SM (shared memory)
     gemm_tc_kernel<<<grid, kGThreads, kGemmSmem, s>>>(g);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
