@@ -356,26 +356,29 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
     OffPair<TI> o_next = load_offsets<TI, MODE, NP>(a, tile + G, num_tiles, warp, lane);
     RowMeta<TI> m = stage_bag<TI, MODE, NP>(a, tile, num_tiles, warp, lane,
                                             load_offsets<TI, MODE, NP>(a, tile, num_tiles, warp, lane));
-    for (; tile < num_tiles; tile += G) {
-        // ---- every single-row source of the warp in flight at once, straight into the operand lines ----
-        // An fp32 row lands unswizzled in the four (D = 128) or two 128-byte lines its hi / lo halves
-        // will occupy and is split there in place; a bf16 row lands at its final, swizzled hi position
-        // (lo = 0).  The warp moves F32_GROUPS (bf16: BF_GROUPS) rows per instruction, 16 bytes a lane.
+    // Every single-row source of the warp's rows of tile `tl` in flight at once, straight into the operand
+    // lines.  An fp32 row lands unswizzled in the four (D = 128) or two 128-byte lines its hi / lo halves will
+    // occupy and is split there in place; a bf16 row lands at its final, swizzled hi position (lo = 0).  The
+    // warp moves F32_GROUPS (bf16: BF_GROUPS) rows per instruction, 16 bytes a lane.
+    auto issue_rows = [&](int64_t tl, const RowMeta<TI>& mm, uint32_t& conv_f32, uint32_t& conv_bf, uint32_t& empty) {
+        // lane group g32 (F32_CHUNKS lanes, one 16-byte chunk each) moves fp32 rows g32 * F32_SLOTS .. + F32_SLOTS - 1
+        const int g32 = lane / F32_CHUNKS, c32 = lane % F32_CHUNKS;
+        unsigned char* const raw_lane = op_hi + (c32 >> 3) * REGION + (c32 & 7) * 16 + (kWarp * warp + g32 * F32_SLOTS) * 128;
         const int rt = kWarp * warp + lane;
         const int k = rt % NP;
-        const int64_t b = tile * S + rt / NP;
+        const int64_t b = tl * S + rt / NP;
         const char* src = nullptr;
         uint32_t bytes = 0;
-        if (m.kind == 1) {
+        if (mm.kind == 1) {
             src = reinterpret_cast<const char*>(a.dense + b * D);
             bytes = F32_BYTES;
-        } else if (m.kind == 2) {
+        } else if (mm.kind == 2) {
             if (MODE == kInteract) {
                 src = reinterpret_cast<const char*>(a.pooled_in + (b * T + (k - 1)) * D);
                 bytes = F32_BYTES;
-            } else if (m.len == 1) {
-                if (m.idx >= 0 && m.idx < tab_rows[k - 1]) {
-                    src = tab_base[k - 1] + static_cast<uint64_t>(m.idx) * TE_BYTES;
+            } else if (mm.len == 1) {
+                if (mm.idx >= 0 && mm.idx < tab_rows[k - 1]) {
+                    src = tab_base[k - 1] + static_cast<uint64_t>(mm.idx) * TE_BYTES;
                     bytes = TE_BYTES;
                 } else {
                     flag_status(a.status, DLRM_ERR_INDEX_OOB);  // contributes zero, still counts in L
@@ -383,12 +386,9 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
             }
         }
         const bool f32row = bytes == F32_BYTES;
-        const uint32_t conv_f32 = __ballot_sync(kFull, bytes != 0 && f32row);
-        const uint32_t conv_bf = __ballot_sync(kFull, bytes != 0 && !f32row);
-        const uint32_t empty = __ballot_sync(kFull, m.kind == 2 && bytes == 0 && (MODE == kInteract || m.len <= 1));
-        // lane group g (F32_CHUNKS lanes, one 16-byte chunk each) moves rows g * SLOTS .. g * SLOTS + SLOTS - 1
-        const int g32 = lane / F32_CHUNKS, c32 = lane % F32_CHUNKS;
-        unsigned char* const raw_lane = op_hi + (c32 >> 3) * REGION + (c32 & 7) * 16 + (kWarp * warp + g32 * F32_SLOTS) * 128;
+        conv_f32 = __ballot_sync(kFull, bytes != 0 && f32row);
+        conv_bf = __ballot_sync(kFull, bytes != 0 && !f32row);
+        empty = __ballot_sync(kFull, mm.kind == 2 && bytes == 0 && (MODE == kInteract || mm.len <= 1));
 #pragma unroll
         for (int q = 0; q < F32_SLOTS; ++q) {
             const int r = g32 * F32_SLOTS + q;
@@ -408,6 +408,24 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
             }
         }
         cp_async_commit();
+    };
+    // One-sample tiles (NP = 128) issue the next tile's rows as soon as this tile's MMAs have read the
+    // operands, so they travel during the epilogue and the output stores (a long phase at N > 64).
+    uint32_t early_f32 = 0, early_bf = 0, early_empty = 0;
+    bool early = false;
+
+    for (; tile < num_tiles; tile += G) {
+        uint32_t conv_f32, conv_bf, empty;
+        if (NP == kTileRows && early) {
+            conv_f32 = early_f32;
+            conv_bf = early_bf;
+            empty = early_empty;
+            early = false;
+        } else {
+            issue_rows(tile, m, conv_f32, conv_bf, empty);
+        }
+        const int g32 = lane / F32_CHUNKS, c32 = lane % F32_CHUNKS;
+        unsigned char* const raw_lane = op_hi + (c32 >> 3) * REGION + (c32 & 7) * 16 + (kWarp * warp + g32 * F32_SLOTS) * 128;
 
         // ---- the next tiles' metadata while these rows travel ----
         const RowMeta<TI> m_next = stage_bag<TI, MODE, NP>(a, tile + G, num_tiles, warp, lane, o_next);
@@ -664,6 +682,10 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
         mma_pending = false;
         mma_phase ^= 1;
         tc::fence_after_sync();
+        if (NP == kTileRows && tile + G < num_tiles) {  // m already holds the next tile's rows
+            issue_rows(tile + G, m, early_f32, early_bf, early_empty);
+            early = true;
+        }
 
         // ---- epilogue: this warp's rows of its sample's diagonal block ----
         {

@@ -363,7 +363,8 @@ __global__ void __launch_bounds__(256) col_sum_kernel(const float* __restrict__ 
     }
 }
 
-// W -= lr * sum_s partial[s] (splits added in order); b -= lr * sum_chunk db_part[chunk] (in order).
+// W -= lr * sum_s partial[s] (splits added in order); b -= lr * sum_chunk db_part[chunk]: a warp per
+// element of b, lane l adding chunks l, l + 32, ... in order, then the lanes' sums by a fixed butterfly.
 __global__ void __launch_bounds__(256) sgd_update_kernel(float* __restrict__ w, const float* __restrict__ partial,
                                                          int splits, int64_t n, float* __restrict__ b,
                                                          const float* __restrict__ db_part, int64_t nb, float lr)
@@ -373,12 +374,17 @@ __global__ void __launch_bounds__(256) sgd_update_kernel(float* __restrict__ w, 
         for (int z = 0; z < splits; ++z) s += partial[static_cast<int64_t>(z) * n + i];
         w[i] = fmaf(-lr, s, w[i]);
     }
-    if (b != nullptr)
-        for (int64_t i = blockIdx.x * int64_t{blockDim.x} + threadIdx.x; i < nb; i += int64_t{gridDim.x} * blockDim.x) {
+    if (b != nullptr) {
+        const int lane = threadIdx.x % kWarp;
+        const int64_t warps = int64_t{gridDim.x} * (blockDim.x / kWarp);
+        for (int64_t i = blockIdx.x * int64_t{blockDim.x / kWarp} + threadIdx.x / kWarp; i < nb; i += warps) {
             float s = 0.0f;
-            for (int q = 0; q < kColChunks; ++q) s += db_part[static_cast<int64_t>(q) * nb + i];
-            b[i] = fmaf(-lr, s, b[i]);
+            for (int q = lane; q < kColChunks; q += kWarp) s += db_part[static_cast<int64_t>(q) * nb + i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            if (lane == 0) b[i] = fmaf(-lr, s, b[i]);
         }
+    }
 }
 
 // ---- head ----------------------------------------------------------------------------------------------
