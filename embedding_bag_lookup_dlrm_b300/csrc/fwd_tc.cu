@@ -293,8 +293,10 @@ __device__ __forceinline__ int pop_rows(uint32_t& mask, int g)
 
 // MULTI: bags of several lookups are pooled by the whole warp from one list of
 // lookups (else one bag at a time, the rare case of a mostly one-hot batch).
+// D = 64 without multi-lookup pooling fits 128 registers (no spills) and 56 KB of shared memory: 4 CTAs per
+// SM instead of 3.
 template <int D, typename TE, typename TI, int MODE, int NP, bool MULTI>
-__global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_constant__ FwdArgs a, int64_t num_tiles)
+__global__ void __launch_bounds__(kThreads, (D == 64 && !MULTI) ? 4 : 3) forward_tc_kernel(const __grid_constant__ FwdArgs a, int64_t num_tiles)
 {
     constexpr int C = D / kWarp;                 // columns per lane when pooling in registers
     constexpr int S = kTileRows / NP;            // samples per tile
@@ -356,14 +358,13 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
     OffPair<TI> o_next = load_offsets<TI, MODE, NP>(a, tile + G, num_tiles, warp, lane);
     RowMeta<TI> m = stage_bag<TI, MODE, NP>(a, tile, num_tiles, warp, lane,
                                             load_offsets<TI, MODE, NP>(a, tile, num_tiles, warp, lane));
-    // Every single-row source of the warp's rows of tile `tl` in flight at once, straight into the operand
-    // lines.  An fp32 row lands unswizzled in the four (D = 128) or two 128-byte lines its hi / lo halves will
-    // occupy and is split there in place; a bf16 row lands at its final, swizzled hi position (lo = 0).  The
-    // warp moves F32_GROUPS (bf16: BF_GROUPS) rows per instruction, 16 bytes a lane.
-    auto issue_rows = [&](int64_t tl, const RowMeta<TI>& mm, uint32_t& conv_f32, uint32_t& conv_bf, uint32_t& empty) {
-        // lane group g32 (F32_CHUNKS lanes, one 16-byte chunk each) moves fp32 rows g32 * F32_SLOTS .. + F32_SLOTS - 1
-        const int g32 = lane / F32_CHUNKS, c32 = lane % F32_CHUNKS;
-        unsigned char* const raw_lane = op_hi + (c32 >> 3) * REGION + (c32 & 7) * 16 + (kWarp * warp + g32 * F32_SLOTS) * 128;
+    // One-sample tiles (NP = 128) issue the next tile's rows as soon as this tile's MMAs have read the
+    // operands, so they travel during the epilogue and the output stores (a long phase at N > 64); the next
+    // iteration then only takes the masks saved here.  (The loop top below stays as it is for every tile
+    // shape: for NP < 128 `pre` is a compile-time false and that code is unchanged.)
+    uint32_t early_f32 = 0, early_bf = 0, early_empty = 0;
+    bool early = false;
+    auto issue_early = [&](int64_t tl, const RowMeta<TI>& mm) {
         const int rt = kWarp * warp + lane;
         const int k = rt % NP;
         const int64_t b = tl * S + rt / NP;
@@ -385,15 +386,16 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
                 }
             }
         }
-        const bool f32row = bytes == F32_BYTES;
-        conv_f32 = __ballot_sync(kFull, bytes != 0 && f32row);
-        conv_bf = __ballot_sync(kFull, bytes != 0 && !f32row);
-        empty = __ballot_sync(kFull, mm.kind == 2 && bytes == 0 && (MODE == kInteract || mm.len <= 1));
+        early_f32 = __ballot_sync(kFull, bytes != 0 && bytes == F32_BYTES);
+        early_bf = __ballot_sync(kFull, bytes != 0 && bytes != F32_BYTES);
+        early_empty = __ballot_sync(kFull, mm.kind == 2 && bytes == 0 && (MODE == kInteract || mm.len <= 1));
+        const int g32 = lane / F32_CHUNKS, c32 = lane % F32_CHUNKS;
+        unsigned char* const raw_lane = op_hi + (c32 >> 3) * REGION + (c32 & 7) * 16 + (kWarp * warp + g32 * F32_SLOTS) * 128;
 #pragma unroll
         for (int q = 0; q < F32_SLOTS; ++q) {
             const int r = g32 * F32_SLOTS + q;
             const char* p = reinterpret_cast<const char*>(shfl64(reinterpret_cast<int64_t>(src), r));
-            if ((conv_f32 >> r) & 1u) cp_async16(raw_lane + q * 128, p + c32 * 16);
+            if ((early_f32 >> r) & 1u) cp_async16(raw_lane + q * 128, p + c32 * 16);
         }
         if (sizeof(TE) == 2) {
             const int gb = lane / BF_CHUNKS, cb = lane % BF_CHUNKS;
@@ -403,29 +405,69 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
                 const int r = gb * BF_SLOTS + q;
                 const int row = kWarp * warp + r;
                 const char* p = reinterpret_cast<const char*>(shfl64(reinterpret_cast<int64_t>(src), r));
-                if ((conv_bf >> r) & 1u)  // straight to the swizzled hi position: a bf16 row is its own hi, lo = 0
-                    cp_async16(hi_lane + row * 128 + (((cb & 7) ^ (r & 7)) << 4), p + cb * 16);
+                if ((early_bf >> r) & 1u) cp_async16(hi_lane + row * 128 + (((cb & 7) ^ (r & 7)) << 4), p + cb * 16);
             }
         }
         cp_async_commit();
+        early = true;
     };
-    // One-sample tiles (NP = 128) issue the next tile's rows as soon as this tile's MMAs have read the
-    // operands, so they travel during the epilogue and the output stores (a long phase at N > 64).
-    uint32_t early_f32 = 0, early_bf = 0, early_empty = 0;
-    bool early = false;
 
     for (; tile < num_tiles; tile += G) {
-        uint32_t conv_f32, conv_bf, empty;
-        if (NP == kTileRows && early) {
-            conv_f32 = early_f32;
-            conv_bf = early_bf;
-            empty = early_empty;
-            early = false;
-        } else {
-            issue_rows(tile, m, conv_f32, conv_bf, empty);
+        const bool pre = NP == kTileRows && early;  // this tile's rows were issued during the last epilogue
+        early = false;
+        // ---- every single-row source of the warp in flight at once, straight into the operand lines ----
+        // An fp32 row lands unswizzled in the four (D = 128) or two 128-byte lines its hi / lo halves
+        // will occupy and is split there in place; a bf16 row lands at its final, swizzled hi position
+        // (lo = 0).  The warp moves F32_GROUPS (bf16: BF_GROUPS) rows per instruction, 16 bytes a lane.
+        const int rt = kWarp * warp + lane;
+        const int k = rt % NP;
+        const int64_t b = tile * S + rt / NP;
+        const char* src = nullptr;
+        uint32_t bytes = 0;
+        if (pre) {
+        } else if (m.kind == 1) {
+            src = reinterpret_cast<const char*>(a.dense + b * D);
+            bytes = F32_BYTES;
+        } else if (m.kind == 2) {
+            if (MODE == kInteract) {
+                src = reinterpret_cast<const char*>(a.pooled_in + (b * T + (k - 1)) * D);
+                bytes = F32_BYTES;
+            } else if (m.len == 1) {
+                if (m.idx >= 0 && m.idx < tab_rows[k - 1]) {
+                    src = tab_base[k - 1] + static_cast<uint64_t>(m.idx) * TE_BYTES;
+                    bytes = TE_BYTES;
+                } else {
+                    flag_status(a.status, DLRM_ERR_INDEX_OOB);  // contributes zero, still counts in L
+                }
+            }
         }
+        const bool f32row = bytes == F32_BYTES;
+        const uint32_t conv_f32 = pre ? early_f32 : __ballot_sync(kFull, bytes != 0 && f32row);
+        const uint32_t conv_bf = pre ? early_bf : __ballot_sync(kFull, bytes != 0 && !f32row);
+        const uint32_t empty =
+            pre ? early_empty : __ballot_sync(kFull, m.kind == 2 && bytes == 0 && (MODE == kInteract || m.len <= 1));
+        // lane group g (F32_CHUNKS lanes, one 16-byte chunk each) moves rows g * SLOTS .. g * SLOTS + SLOTS - 1
         const int g32 = lane / F32_CHUNKS, c32 = lane % F32_CHUNKS;
         unsigned char* const raw_lane = op_hi + (c32 >> 3) * REGION + (c32 & 7) * 16 + (kWarp * warp + g32 * F32_SLOTS) * 128;
+#pragma unroll
+        for (int q = 0; q < F32_SLOTS; ++q) {
+            const int r = g32 * F32_SLOTS + q;
+            const char* p = reinterpret_cast<const char*>(shfl64(reinterpret_cast<int64_t>(src), r));
+            if (!pre && ((conv_f32 >> r) & 1u)) cp_async16(raw_lane + q * 128, p + c32 * 16);
+        }
+        if (sizeof(TE) == 2) {
+            const int gb = lane / BF_CHUNKS, cb = lane % BF_CHUNKS;
+            unsigned char* const hi_lane = op_hi + (cb >> 3) * REGION;
+#pragma unroll
+            for (int q = 0; q < BF_SLOTS; ++q) {
+                const int r = gb * BF_SLOTS + q;
+                const int row = kWarp * warp + r;
+                const char* p = reinterpret_cast<const char*>(shfl64(reinterpret_cast<int64_t>(src), r));
+                if (!pre && ((conv_bf >> r) & 1u))  // straight to the swizzled hi position: a bf16 row is its own hi, lo = 0
+                    cp_async16(hi_lane + row * 128 + (((cb & 7) ^ (r & 7)) << 4), p + cb * 16);
+            }
+        }
+        if (!pre) cp_async_commit();
 
         // ---- the next tiles' metadata while these rows travel ----
         const RowMeta<TI> m_next = stage_bag<TI, MODE, NP>(a, tile + G, num_tiles, warp, lane, o_next);
@@ -682,9 +724,8 @@ __global__ void __launch_bounds__(kThreads, 3) forward_tc_kernel(const __grid_co
         mma_pending = false;
         mma_phase ^= 1;
         tc::fence_after_sync();
-        if (NP == kTileRows && tile + G < num_tiles) {  // m already holds the next tile's rows
-            issue_rows(tile + G, m, early_f32, early_bf, early_empty);
-            early = true;
+        if constexpr (NP == kTileRows) {
+            if (tile + G < num_tiles) issue_early(tile + G, m);  // m already holds the next tile's rows
         }
 
         // ---- epilogue: this warp's rows of its sample's diagonal block ----
