@@ -334,32 +334,65 @@ __global__ void __launch_bounds__(256) split_rows_kernel(const float* __restrict
     }
 }
 
-// Column sums of src [R x C] (times [mask > 0]) over row chunks: part[chunk][c]; a fixed order.  Enough
-// chunks that the batch's columns keep every SM busy (4,096 blocks for C = 512).
+// The backward's dz = src * [mask > 0] split into hi / lo [R x Kp] (as split_rows_kernel does) and, in the
+// same pass, its column sums over row chunks, part[chunk][c] (the bias gradient's partials, added in chunk
+// order by the update): per column, row lane ty adds rows r_lo + ty, + 8, ... of the chunk in order, then
+// the 8 row lanes are added in order.  A block holds 32 groups of 8 columns x 8 row lanes; enough chunks
+// that the batch keeps every SM busy.
 constexpr int kColChunks = 256;
-__global__ void __launch_bounds__(256) col_sum_kernel(const float* __restrict__ src, const float* __restrict__ mask,
-                                                      int64_t R, int64_t C, float* __restrict__ part)
+__global__ void __launch_bounds__(256) split_rows_colsum_kernel(const float* __restrict__ src,
+                                                                const float* __restrict__ mask, int64_t ld, int64_t R,
+                                                                int64_t K, int64_t Kp, int vec,
+                                                                __nv_bfloat16* __restrict__ hi,
+                                                                __nv_bfloat16* __restrict__ lo, float* __restrict__ part)
 {
-    __shared__ float acc[8][33];
+    __shared__ float acc[8][32 * 8 + 1];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + tx;
+    const int64_t k0 = (static_cast<int64_t>(blockIdx.x) * 32 + tx) * 8;
     const int64_t per = (R + kColChunks - 1) / kColChunks;
     const int64_t r_lo = static_cast<int64_t>(blockIdx.y) * per, r_hi = min(R, r_lo + per);
-    float s = 0.0f;
-    if (c < C)
-#pragma unroll 4
+    float sum[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum[i] = 0.0f;
+    if (k0 < Kp) {
         for (int64_t r = r_lo + ty; r < r_hi; r += 8) {
-            float v = src[r * C + c];
-            if (mask != nullptr && !(mask[r * C + c] > 0.0f)) v = 0.0f;
-            s += v;
+            const float* sr = src + r * ld + k0;
+            const float* mr = mask != nullptr ? mask + r * ld + k0 : nullptr;
+            float v[8];
+            if (vec && k0 + 8 <= K) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(sr)), b = __ldg(reinterpret_cast<const float4*>(sr) + 1);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+                if (mr != nullptr) {
+                    const float4 c = __ldg(reinterpret_cast<const float4*>(mr)), d = __ldg(reinterpret_cast<const float4*>(mr) + 1);
+                    const float m[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (!(m[i] > 0.0f)) v[i] = 0.0f;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = k0 + i < K ? __ldg(sr + i) : 0.0f;
+                    if (mr != nullptr && k0 + i < K && !(__ldg(mr + i) > 0.0f)) v[i] = 0.0f;
+                }
+            }
+            uint4 h, l;
+            split8(v, h, l);
+            reinterpret_cast<uint4*>(hi + r * Kp + k0)[0] = h;
+            reinterpret_cast<uint4*>(lo + r * Kp + k0)[0] = l;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum[i] += v[i];
         }
-    acc[ty][tx] = s;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[ty][tx * 8 + i] = sum[i];
     __syncthreads();
-    if (ty == 0 && c < C) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    if (c < K) {
         float t = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) t += acc[q][tx];
-        part[static_cast<int64_t>(blockIdx.y) * C + c] = t;
+        for (int q = 0; q < 8; ++q) t += acc[q][threadIdx.x];
+        part[static_cast<int64_t>(blockIdx.y) * K + c] = t;
     }
 }
 
@@ -680,7 +713,14 @@ dlrm_status launch_fc_bwd_sgd(const float* x, float* w, float* b, const float* y
     const BwdWs ws = carve_bwd(workspace, M, K, N, nullptr);
     const int64_t np = pad8(N), kp = pad8(K);
     const float* mask = relu ? y : nullptr;
-    split_rows(dy, mask, N, M, N, np, ws.dzh, ws.dzl, s);  // dz = dy [y > 0], [M x N]
+    if (b != nullptr) {  // dz = dy [y > 0], [M x N], and the partials of db = sum over the batch of dz
+        const auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+        const int vec = N % 4 == 0 && a16(dy) && (mask == nullptr || a16(mask));
+        const dim3 grid(static_cast<unsigned>((np / 8 + 31) / 32), kColChunks);
+        split_rows_colsum_kernel<<<grid, 256, 0, s>>>(dy, mask, N, M, N, np, vec, ws.dzh, ws.dzl, ws.db_part);
+    } else {
+        split_rows(dy, mask, N, M, N, np, ws.dzh, ws.dzl, s);
+    }
     split_rows(x, nullptr, K, M, K, kp, ws.xh, ws.xl, s);  // x [M x K]
     // dx = dz W: A = dz [M x N] K-major; B[k][n] = W[n][k]: W [N x K] read MN-major
     if (dx != nullptr) {
@@ -693,10 +733,6 @@ dlrm_status launch_fc_bwd_sgd(const float* x, float* w, float* b, const float* y
     const Operand A{ws.dzh, ws.dzl, np, M, 1}, B{ws.xh, ws.xl, kp, M, 1};
     dlrm_status st = launch_gemm(A, B, nullptr, ws.part, K, N, K, M, 0, ws.splits, static_cast<int64_t>(N) * K, status, s);
     if (st != DLRM_OK) return st;
-    if (b != nullptr) {
-        const dim3 grid(static_cast<unsigned>((N + 31) / 32), kColChunks);
-        col_sum_kernel<<<grid, 256, 0, s>>>(dy, mask, M, N, ws.db_part);
-    }
     const int64_t n = static_cast<int64_t>(N) * K;
     const int64_t blocks = (n + 255) / 256;
     sgd_update_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(
