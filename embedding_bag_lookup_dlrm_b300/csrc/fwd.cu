@@ -35,6 +35,15 @@
 namespace dlrm {
 namespace {
 
+// lo += low bf16 half of w, hi += high half: add.f32.bf16 converts the bf16 operand to fp32 exactly and
+// rounds the sum once, as an fp32 add of the widened value would.
+__device__ __forceinline__ void add_bf16_pair(float& lo, float& hi, uint32_t w)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w));
+}
+
 // Shared-memory layout of one group (byte offsets), shared by host and device.
 struct GroupLayout {
     int T, N, NPAD, NB, K, S;  // S = fp32 row stride of V (D + 4)
@@ -130,6 +139,14 @@ __device__ void pool_bag_warp(const TE* __restrict__ table, int64_t V_t, const v
                 if (!ok[u]) continue;
 #pragma unroll
                 for (int k = 0; k < CPL; ++k) {
+                    if constexpr (sizeof(TE) == 2) {
+                        // mixed-precision adds (add.f32.bf16): the bf16 element, widened exactly, plus the fp32
+                        // sum, rounded once; the same result as widening first, in one instruction per element
+                        const uint32_t w[4] = {raw[u][k].x, raw[u][k].y, raw[u][k].z, raw[u][k].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) add_bf16_pair(acc[k][2 * e], acc[k][2 * e + 1], w[e]);
+                        continue;
+                    }
                     // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
                     float f[EPC];
                     if constexpr (sizeof(TE) == 4) {
