@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pool.cuh"
 
 namespace dlrm {
 namespace {
@@ -336,26 +337,18 @@ __global__ void __launch_bounds__(kBagThreads, 2) embbag_list_kernel(const __gri
                     if (!valid) continue;
 #pragma unroll
                     for (int k = 0; k < NP; ++k) {
-                        float f[NE];
-                        if constexpr (sizeof(TE) == 4) {
+                        if constexpr (sizeof(TE) == 2) {  // mixed-precision adds, one per element
 #pragma unroll
-                            for (int e = 0; e < NE; ++e) f[e] = __uint_as_float(raw[u][k].w(e));
+                            for (int e = 0; e < NE / 2; ++e) add_bf16_pair(acc[k][2 * e], acc[k][2 * e + 1], raw[u][k].w(e));
+                        } else if constexpr (NE == 1) {
+                            acc[k][0] += __uint_as_float(raw[u][k].w(0));
                         } else {
-#pragma unroll
-                            for (int e = 0; e < NE / 2; ++e) {
-                                const uint32_t x = raw[u][k].w(e);
-                                f[2 * e] = __uint_as_float(x << 16);
-                                f[2 * e + 1] = __uint_as_float(x & 0xffff0000u);
-                            }
-                        }
-                        // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
-                        if constexpr (NE == 1) {
-                            acc[k][0] += f[0];
-                        } else {
+                            // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
 #pragma unroll
                             for (int e = 0; e < NE; e += 2) {
                                 const float2 r2 = __fadd2_rn(make_float2(acc[k][e], acc[k][e + 1]),
-                                                             make_float2(f[e], f[e + 1]));
+                                                             make_float2(__uint_as_float(raw[u][k].w(e)),
+                                                                         __uint_as_float(raw[u][k].w(e + 1))));
                                 acc[k][e] = r2.x;
                                 acc[k][e + 1] = r2.y;
                             }

@@ -31,18 +31,10 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pool.cuh"
 
 namespace dlrm {
 namespace {
-
-// lo += low bf16 half of w, hi += high half: add.f32.bf16 converts the bf16 operand to fp32 exactly and
-// rounds the sum once, as an fp32 add of the widened value would.
-__device__ __forceinline__ void add_bf16_pair(float& lo, float& hi, uint32_t w)
-{
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
-        : "+f"(lo), "+f"(hi)
-        : "r"(w));
-}
 
 // Shared-memory layout of one group (byte offsets), shared by host and device.
 struct GroupLayout {
@@ -145,23 +137,16 @@ __device__ void pool_bag_warp(const TE* __restrict__ table, int64_t V_t, const v
                         const uint32_t w[4] = {raw[u][k].x, raw[u][k].y, raw[u][k].z, raw[u][k].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) add_bf16_pair(acc[k][2 * e], acc[k][2 * e + 1], w[e]);
-                        continue;
-                    }
-                    // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
-                    float f[EPC];
-                    if constexpr (sizeof(TE) == 4) {
-                        f[0] = __uint_as_float(raw[u][k].x);
-                        f[1] = __uint_as_float(raw[u][k].y);
-                        f[2] = __uint_as_float(raw[u][k].z);
-                        f[3] = __uint_as_float(raw[u][k].w);
                     } else {
-                        bf16x8_to_f32(raw[u][k], f);
-                    }
-#pragma unroll
-                    for (int e = 0; e < EPC; e += 2) {
-                        const float2 s2 = __fadd2_rn(make_float2(acc[k][e], acc[k][e + 1]), make_float2(f[e], f[e + 1]));
-                        acc[k][e] = s2.x;
-                        acc[k][e + 1] = s2.y;
+                        // packed adds (add.f32x2): each lane an ordinary fp32 add, rounded once
+                        const float2 s0 = __fadd2_rn(make_float2(acc[k][0], acc[k][1]),
+                                                     make_float2(__uint_as_float(raw[u][k].x), __uint_as_float(raw[u][k].y)));
+                        const float2 s1 = __fadd2_rn(make_float2(acc[k][2], acc[k][3]),
+                                                     make_float2(__uint_as_float(raw[u][k].z), __uint_as_float(raw[u][k].w)));
+                        acc[k][0] = s0.x;
+                        acc[k][1] = s0.y;
+                        acc[k][2] = s1.x;
+                        acc[k][3] = s1.y;
                     }
                 }
             }
