@@ -23,8 +23,8 @@ constexpr uint32_t kSentinel = 0xFFFFFFFFu;  // key of a lookup that updates not
 
 // ---- workspace layout ------------------------------------------------------
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 8;
-constexpr int kSortTile = kSortThreads * kSortItems;  // 2048 keys per tile
+constexpr int kSortItems = 16;
+constexpr int kSortTile = kSortThreads * kSortItems;  // 4096 keys per tile
 constexpr int kMaxRadixBits = 9;  // digit width of a pass: up to 9 bits
 constexpr int kMaxBins = 1 << kMaxRadixBits;
 constexpr int kChunk = 128;  // sorted lookups per segment-reduction warp
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(256) expand_keys_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 // 3. Stable LSD radix sort of (key, value) pairs by key, up to 9 bits per pass
 //    (digits of `dbits` bits, bins = 2^dbits):
-//    hist:    digit counts per tile of 2048 pairs   -> counts[digit][tile]
+//    hist:    digit counts per tile of 4096 pairs   -> counts[digit][tile]
 //    scan:    per digit, exclusive scan over tiles; digit totals
 //    scatter: rank each pair among equal digits of its tile (earlier
 //             positions first), reorder the tile by digit in shared memory,
@@ -448,7 +448,7 @@ struct ScatterSmem {
     uint32_t val[kSortTile];
 };
 
-__global__ void __launch_bounds__(kSortThreads, 4) radix_scatter_kernel(
+__global__ void __launch_bounds__(kSortThreads, 2) radix_scatter_kernel(
     const uint32_t* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, uint32_t* __restrict__ keys_out,
     uint32_t* __restrict__ vals_out, int64_t n, int shift, int dbits, const uint32_t* __restrict__ counts,
     int64_t num_tiles, const uint32_t* __restrict__ bin_total)

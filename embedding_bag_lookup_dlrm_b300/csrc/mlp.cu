@@ -483,35 +483,36 @@ __global__ void __launch_bounds__(kHeadThreads) head_kernel(const float* __restr
     }
 }
 
-// Sums the blocks' partials in block order; loss = sum / M; w -= lr dw; b -= lr db.  A block per 32
-// columns of w: warp q adds blocks q, q + 8, ..., then the 8 warp sums are added in warp order.
+// Sums the blocks' partials; loss = sum / M; w -= lr dw; b -= lr db.  A warp per element of w (warp K:
+// db and the loss): lane l adds blocks l, l + 32, ... in order, then the lanes' sums by a fixed butterfly.
 __global__ void __launch_bounds__(256) head_update_kernel(float* __restrict__ w, float* __restrict__ b,
                                                           const float* __restrict__ part_w,
                                                           const float* __restrict__ part_s, int blocks, int in_dim,
                                                           int64_t M, float lr, float* __restrict__ loss)
 {
-    __shared__ float acc[8][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int k = blockIdx.x * 32 + tx;
-    float s = 0.0f;
-    if (k < in_dim)
-        for (int q = ty; q < blocks; q += 8) s += part_w[static_cast<int64_t>(q) * in_dim + k];
-    acc[ty][tx] = s;
-    __syncthreads();
-    if (ty == 0 && k < in_dim) {
-        float t = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) t += acc[q][tx];
-        w[k] = fmaf(-lr, t, w[k]);
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        float db = 0.0f, l = 0.0f;
-        for (int q = 0; q < blocks; ++q) {
-            db += part_s[2 * q];
-            l += part_s[2 * q + 1];
+    const int lane = threadIdx.x % kWarp;
+    const int k = static_cast<int>(blockIdx.x) * (blockDim.x / kWarp) + static_cast<int>(threadIdx.x / kWarp);
+    if (k > in_dim) return;
+    float s0 = 0.0f, s1 = 0.0f;
+    for (int q = lane; q < blocks; q += kWarp) {
+        if (k < in_dim) {
+            s0 += part_w[static_cast<int64_t>(q) * in_dim + k];
+        } else {
+            s0 += part_s[2 * q];
+            s1 += part_s[2 * q + 1];
         }
-        b[0] = fmaf(-lr, db, b[0]);
-        if (loss != nullptr) loss[0] = l / static_cast<float>(M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(kFull, s0, o);
+        s1 += __shfl_xor_sync(kFull, s1, o);
+    }
+    if (lane != 0) return;
+    if (k < in_dim) {
+        w[k] = fmaf(-lr, s0, w[k]);
+    } else {
+        b[0] = fmaf(-lr, s0, b[0]);
+        if (loss != nullptr) loss[0] = s1 / static_cast<float>(M);
     }
 }
 
@@ -757,8 +758,8 @@ dlrm_status launch_head(const float* h, float* w, float* b, const float* label, 
                                              align256(sizeof(float) * static_cast<size_t>(blocks) * K));
     head_kernel<<<static_cast<unsigned>(blocks), kHeadThreads, 0, s>>>(h, w, b, label, M, K, kHeadRowsPerBlock, prob,
                                                                        dh, part_w, part_s);
-    head_update_kernel<<<static_cast<unsigned>((K + 31) / 32), 256, 0, s>>>(w, b, part_w, part_s,
-                                                                            static_cast<int>(blocks), K, M, lr, loss);
+    head_update_kernel<<<static_cast<unsigned>((K + 1 + 7) / 8), 256, 0, s>>>(w, b, part_w, part_s,
+                                                                               static_cast<int>(blocks), K, M, lr, loss);
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
