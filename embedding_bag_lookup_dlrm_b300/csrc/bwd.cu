@@ -801,6 +801,7 @@ __global__ void __launch_bounds__(kSegThreads, SegRing<D>::kMinBlocks) segment_c
 #pragma unroll
     for (int j = 0; j < R - 1; ++j) issue(j, j);
     int rs = 0, ws = R - 1;  // the slot read now, the slot refilled now
+#pragma unroll 2
     for (int j = 0; j < live; ++j) {
         seg_wait<R - 2>();  // this lookup's group has landed
         const int t = ring.table[j];
