@@ -68,9 +68,18 @@ def parse():
     p.add_argument("--model", action="store_true",
                    help="the whole DLRM training step on the training workload: bottom MLP 13-512-256-D, the sparse "
                         "path, top MLP (D+K)-512-256, a 256-1 sigmoid head with BCE; SGD on the MLPs")
+    p.add_argument("--sort-in-backward", action="store_true",
+                   help="training workload: the backward's key build and sort run inside the backward call, beside "
+                        "the interaction backward, instead of beside the forward (dlrm_sparse_bwd_sort)")
+    p.add_argument("--side-priority", choices=["high", "low"], default=None,
+                   help="priority of the training step's side stream (key build and sort); default low when the "
+                        "sort runs beside the forward, high when it runs inside the backward")
     p.add_argument("--hash", action="store_true",
                    help="the bags arrive as raw 64-bit IDs: the hashing pre-pass (ID mod V_t) runs in each step")
-    return p.parse_args()
+    args = p.parse_args()
+    if args.side_priority is None:
+        args.side_priority = "high" if args.sort_in_backward else "low"
+    return args
 
 
 def dist_env():
@@ -559,9 +568,10 @@ def run_ours(args, w):
     torch.cuda.synchronize()
 
     s = torch.cuda.Stream(device=dev)
-    # the training step's key build and sort run beside its interaction backward, on a stream of the
-    # highest priority so that the short dependent sort kernels get SMs as soon as any free up
-    side = torch.cuda.Stream(device=dev, priority=-100)
+    # the training step's key build and sort run beside its forward and interaction backward, on a stream
+    # of the highest priority (or, --side-priority low, the lowest) so that the short dependent sort kernels
+    # get SMs as soon as any free up
+    side = torch.cuda.Stream(device=dev, priority=0 if args.side_priority == "low" else -100)
 
     def step(i, rec):
         """Queue step i on stream s; rec(name) records the end of a phase."""
@@ -587,10 +597,24 @@ def run_ours(args, w):
             dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, stream=s)
             rec("forward")
             return
+        if args.sort_in_backward:
+            dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, pooled_save=pooled, stream=s)
+            rec("forward")
+            dl.dlrm_sparse_bwd_update(tables, idx, off, x, pooled, grads[k], args.rule, w.lr, w.eps, accum, w.mode,
+                                      grad_dense=grad_dense, workspace=workspace, stream=s, side_stream=side)
+            rec("backward")
+            return
+        # the sort depends only on the bags: it runs on the side stream beside the forward and the
+        # interaction backward; only the backward's per-row sums wait for it
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork.record(s)
+        side.wait_event(fork)
+        dl.dlrm_sparse_bwd_sort(tables, idx, off, workspace, stream=side)
+        join.record(side)
         dl.dlrm_sparse_fwd(tables, idx, off, x, w.mode, out=out, pooled_save=pooled, stream=s)
         rec("forward")
-        dl.dlrm_sparse_bwd_update(tables, idx, off, x, pooled, grads[k], args.rule, w.lr, w.eps, accum, w.mode,
-                                  grad_dense=grad_dense, workspace=workspace, stream=s, side_stream=side)
+        dl.dlrm_sparse_bwd_update_sorted(tables, idx, off, x, pooled, grads[k], args.rule, w.lr, w.eps, accum,
+                                         w.mode, grad_dense=grad_dense, workspace=workspace, sorted=join, stream=s)
         rec("backward")
 
     with torch.cuda.stream(s):
@@ -734,8 +758,12 @@ def phase_is_traced(args, phase) -> bool:
 
 def kernel_of_phase(args, w, phase) -> str:
     return {"forward": forward_kernel_name(w),
-            "backward": "dlrm_sparse_bwd_update kernels (interaction backward, keys, radix sort, row updates; "
-                        f"{args.rule})",
+            "backward": ("dlrm_sparse_bwd_update kernels (interaction backward, keys, radix sort, row updates; "
+                         f"{args.rule})" if args.sort_in_backward else
+                         "dlrm_sparse_bwd_update_sorted kernels (interaction backward, row updates; "
+                         f"{args.rule}); the key build and radix sort run on a low-priority second stream from the "
+                         "step's start, beside the forward and the interaction backward, so the two phases share "
+                         "their time (step_frac is the whole step's bytes over its time)"),
             "hash": "hash_kernel (raw ID mod V_t)",
             "stage": "stage_kernel (cache slots, misses copied from host memory)",
             "lookup": "embbag_kernel (embedding-bag lookup, a lane group per bag"
@@ -847,9 +875,19 @@ def run_e2e_train(args, w, tables, batches, dev, dl, torch, world, side):
         hi = host[i % N_ROTATE][0]
         di, do, dx, dg = stages[k]
         comp.wait_event(copied[k])
-        dl.dlrm_sparse_fwd(tables, di[:hi.numel()], do, dx, w.mode, out=out, pooled_save=pooled, stream=comp)
-        dl.dlrm_sparse_bwd_update(tables, di[:hi.numel()], do, dx, pooled, dg, args.rule, w.lr, w.eps, accum,
-                                  w.mode, grad_dense=gd, workspace=ws, stream=comp, side_stream=side)
+        if args.sort_in_backward:
+            dl.dlrm_sparse_fwd(tables, di[:hi.numel()], do, dx, w.mode, out=out, pooled_save=pooled, stream=comp)
+            dl.dlrm_sparse_bwd_update(tables, di[:hi.numel()], do, dx, pooled, dg, args.rule, w.lr, w.eps, accum,
+                                      w.mode, grad_dense=gd, workspace=ws, stream=comp, side_stream=side)
+        else:  # the sort beside the forward, as in the device-timed step
+            fork, join = torch.cuda.Event(), torch.cuda.Event()
+            fork.record(comp)
+            side.wait_event(fork)
+            dl.dlrm_sparse_bwd_sort(tables, di[:hi.numel()], do, ws, stream=side)
+            join.record(side)
+            dl.dlrm_sparse_fwd(tables, di[:hi.numel()], do, dx, w.mode, out=out, pooled_save=pooled, stream=comp)
+            dl.dlrm_sparse_bwd_update_sorted(tables, di[:hi.numel()], do, dx, pooled, dg, args.rule, w.lr, w.eps,
+                                             accum, w.mode, grad_dense=gd, workspace=ws, sorted=join, stream=comp)
         with torch.cuda.stream(comp):
             gd_host[k].copy_(gd, non_blocking=True)
         ev = torch.cuda.Event()
@@ -961,7 +999,8 @@ def run_model(args, w):
     accum = [torch.full((V,), w.accum_init, dtype=torch.float32, device=dev) for V in w.num_rows]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream(device=dev)
-    side = torch.cuda.Stream(device=dev, priority=-100)
+    # the sparse backward's key build and sort run there, beside the step up to the per-row sums
+    side = torch.cuda.Stream(device=dev, priority=0 if args.side_priority == "low" else -100)
 
     def step(i, rec):
         dense_in, label, idx, off = dev_b[i % N_ROTATE]

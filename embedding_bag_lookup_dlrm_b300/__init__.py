@@ -35,6 +35,7 @@ _ITYPES = {torch.int32: 0, torch.int64: 1}
 
 C_SYMBOLS = ("dlrm_embbag_fwd", "dlrm_interact_fwd", "dlrm_sparse_fwd", "dlrm_sparse_fwd_host",
              "dlrm_sparse_bwd_workspace_size", "dlrm_sparse_bwd_adagrad", "dlrm_sparse_bwd_update",
+             "dlrm_sparse_bwd_sort", "dlrm_sparse_bwd_update_sorted",
              "dlrm_interact_bwd", "dlrm_embbag_bwd_workspace_size", "dlrm_embbag_bwd_update", "dlrm_hash_indices",
              "dlrm_pooled_exchange", "dlrm_tier_init", "dlrm_tier_cache_fill", "dlrm_tier_stage",
              "dlrm_fc_fwd_workspace_size", "dlrm_fc_fwd", "dlrm_fc_bwd_workspace_size", "dlrm_fc_bwd_sgd",
@@ -97,6 +98,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                      ctypes.c_float, P, ctypes.c_size_t, P, P, P], i32),
         "dlrm_sparse_bwd_update": ([T, B, i32, P, P, P, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P,
                                     P], i32),
+        "dlrm_sparse_bwd_sort": ([T, B, P, ctypes.c_size_t, P, P], i32),
+        "dlrm_sparse_bwd_update_sorted": ([T, B, i32, P, P, P, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t,
+                                           P, P, P], i32),
         "dlrm_interact_bwd": ([P, P, P, i64, i32, i32, P, P, P], i32),
         "dlrm_embbag_bwd_workspace_size": ([T, B, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
         "dlrm_embbag_bwd_update": ([T, B, i32, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P, P], i32),
@@ -434,6 +438,52 @@ def dlrm_sparse_bwd_update(tables, indices, offsets, dense, pooled_saved, grad_o
     return grad_dense
 
 
+def dlrm_sparse_bwd_sort(tables, indices, offsets, workspace, status=None, stream=None):
+    """The lookup keys of the bags sorted by row into `workspace` (a training-step workspace of at least
+    dlrm_sparse_bwd_workspace_size bytes), for a later dlrm_sparse_bwd_update_sorted on the same bags."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    _check_cuda(workspace, "workspace")
+    bags = _bags(indices, offsets, B)
+    dev = _device(*tb.tensors, indices, offsets, workspace, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_bwd_sort(ctypes.byref(tb.c), ctypes.byref(bags), workspace.data_ptr(), workspace.numel(),
+                                      status.data_ptr() if status is not None else None, _stream_ptr(stream, dev))
+    _raise(st, "dlrm_sparse_bwd_sort")
+    return workspace
+
+
+def dlrm_sparse_bwd_update_sorted(tables, indices, offsets, dense, pooled_saved, grad_out, rule, lr, eps=0.0,
+                                  accum=None, mode="sum", grad_dense=None, workspace=None, status=None, sorted=None,
+                                  stream=None):
+    """dlrm_sparse_bwd_update on a workspace that dlrm_sparse_bwd_sort filled for the same bags (queued
+    before this call).  sorted: a torch.cuda.Event recorded after the sort on its stream, waited for before
+    the per-row sums only (None: the caller ordered the sort before this call).  Returns grad_dense [B, D]."""
+    lib = load_library()
+    tb = _tables(tables)
+    B = _batch(offsets, tb.T)
+    for name, t in (("dense", dense), ("pooled_saved", pooled_saved), ("grad_out", grad_out)):
+        _check_cuda(t, name, torch.float32)
+    upd, _keep = _update(tb, rule, lr, eps, accum)
+    if grad_dense is None:
+        grad_dense = torch.empty((B, tb.D), dtype=torch.float32, device=dense.device)
+    _check_cuda(grad_dense, "grad_dense", torch.float32)
+    _check_cuda(workspace, "workspace")
+    bags = _bags(indices, offsets, B)
+    dev = _device(*tb.tensors, *(accum or []), indices, offsets, dense, pooled_saved, grad_out, grad_dense,
+                  workspace, status)
+    with torch.cuda.device(dev):
+        st = lib.dlrm_sparse_bwd_update_sorted(ctypes.byref(tb.c), ctypes.byref(bags), _MODES[mode],
+                                               dense.data_ptr(), pooled_saved.data_ptr(), grad_out.data_ptr(),
+                                               grad_dense.data_ptr(), ctypes.byref(upd), workspace.data_ptr(),
+                                               workspace.numel(), status.data_ptr() if status is not None else None,
+                                               sorted.cuda_event if sorted is not None else None,
+                                               _stream_ptr(stream, dev))
+    _raise(st, "dlrm_sparse_bwd_update_sorted")
+    return grad_dense
+
+
 def dlrm_interact_bwd(dense, pooled, grad_out, grad_dense=None, grad_pooled=None, stream=None):
     """The interaction backward alone: (grad_dense [B, D], grad_pooled [B, T, D]); no bag lengths applied."""
     lib = load_library()
@@ -722,8 +772,9 @@ class DLRMModel:
             self._buf[key] = t
         return t
 
-    def forward(self, dense_in, indices, offsets, mode="sum", stream=None, after=None):
-        """Bottom MLP, sparse forward (pooled vectors saved), top MLP; returns the top MLP's output."""
+    def forward(self, dense_in, indices, offsets, mode="sum", stream=None, after=None, before_sparse=None):
+        """Bottom MLP, sparse forward (pooled vectors saved), top MLP; returns the top MLP's output.
+        before_sparse: called once the bottom MLP is queued, before the sparse forward."""
         B = dense_in.shape[0]
         h = dense_in
         self.bot_in = [h]
@@ -738,6 +789,8 @@ class DLRMModel:
         N = self.tables.T + 1
         out = self._get("out", (B, self.tables.D + N * (N - 1) // 2))
         pooled = self._get("pooled", (B, self.tables.T, self.tables.D))
+        if before_sparse:
+            before_sparse()
         dlrm_sparse_fwd(self.tables, indices, offsets, x, mode, out=out, pooled_save=pooled, stream=stream)
         if after:
             after("sparse_fwd")
@@ -754,9 +807,23 @@ class DLRMModel:
 
     def train_step(self, dense_in, indices, offsets, label, lr_mlp, lr_emb, eps=1e-8, accum=None, rule="adagrad",
                    mode="sum", stream=None, side_stream=None, after=None):
-        """One training step; returns (loss [1], prob [B]) as device tensors."""
+        """One training step; returns (loss [1], prob [B]) as device tensors.  With side_stream the lookup-key
+        build and sort of the sparse backward run there (they depend only on the bags), from the sparse
+        forward on, beside everything up to the sparse backward's per-row sums (the bottom MLP's short GEMMs,
+        which the sort's blocks would delay, run before it); without it they run inside the sparse backward."""
         B = dense_in.shape[0]
-        g = self.forward(dense_in, indices, offsets, mode, stream, after)
+        ws = self._ws("ws_sparse", dlrm_sparse_bwd_workspace_size(self.tables, indices, offsets))
+        sorted_ev = torch.cuda.Event() if side_stream is not None else None
+
+        def sort_beside():
+            fork = torch.cuda.Event()
+            fork.record(stream if stream is not None else torch.cuda.current_stream(dense_in.device))
+            side_stream.wait_event(fork)
+            dlrm_sparse_bwd_sort(self.tables, indices, offsets, ws, stream=side_stream)
+            sorted_ev.record(side_stream)
+
+        g = self.forward(dense_in, indices, offsets, mode, stream, after,
+                         before_sparse=sort_beside if side_stream is not None else None)
         w, b = self.head
         prob, loss, dh = dlrm_head_bce_sgd(g, w, b, label, lr_mlp, prob=self._get("prob", (B,)),
                                            loss=self._get("loss", (1,)), dh=self._get("dh", (B, w.shape[0])),
@@ -774,9 +841,13 @@ class DLRMModel:
             after("top_bwd")
         x = self.bot_in[-1]
         gx = self._get("grad_x", (B, self.tables.D))
-        ws = self._ws("ws_sparse", dlrm_sparse_bwd_workspace_size(self.tables, indices, offsets))
-        dlrm_sparse_bwd_update(self.tables, indices, offsets, x, self._buf["pooled"], dy, rule, lr_emb, eps, accum,
-                               mode, grad_dense=gx, workspace=ws, stream=stream, side_stream=side_stream)
+        if sorted_ev is not None:
+            dlrm_sparse_bwd_update_sorted(self.tables, indices, offsets, x, self._buf["pooled"], dy, rule, lr_emb,
+                                          eps, accum, mode, grad_dense=gx, workspace=ws, sorted=sorted_ev,
+                                          stream=stream)
+        else:
+            dlrm_sparse_bwd_update(self.tables, indices, offsets, x, self._buf["pooled"], dy, rule, lr_emb, eps,
+                                   accum, mode, grad_dense=gx, workspace=ws, stream=stream)
         if after:
             after("sparse_bwd")
         dy = gx

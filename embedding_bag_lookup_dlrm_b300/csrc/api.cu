@@ -195,18 +195,10 @@ dlrm_status dlrm_embbag_bwd_workspace_size(const dlrm_tables* tables, const dlrm
 
 namespace {
 
-// Checks shared by the row-update entry points; fills everything of the
-// parameter block but the interaction inputs.
-dlrm_status pack_update(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
-                        const dlrm_update* upd, void* workspace, int32_t* status_dev)
+// The 32-bit limits of the sort and the parameters the lookup keys need
+// (tables, row counts and bases, bags); checked tables and bags.
+dlrm_status pack_rows(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* bags, int32_t* status_dev)
 {
-    dlrm_status st = check_tables(tables);
-    if (st != DLRM_OK) return st;
-    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
-    if (tables->dtype != DLRM_F32) return DLRM_ERR_UNSUPPORTED;
-    if (!mode_ok(mode) || upd == nullptr || workspace == nullptr || !aligned16(workspace)) return DLRM_ERR_INVALID_ARG;
-    if (upd->rule != DLRM_RULE_ADAGRAD && upd->rule != DLRM_RULE_SGD) return DLRM_ERR_INVALID_ARG;
-    if (upd->rule == DLRM_RULE_ADAGRAD && upd->accum == nullptr) return DLRM_ERR_INVALID_ARG;
     int64_t total_rows = 0;
     for (int i = 0; i < tables->num_tables; ++i) total_rows += tables->num_rows[i];
     // 32-bit sort keys (global row ids, the sentinel 2^32 - 1 above them), 32-bit sort values (dP row
@@ -217,10 +209,6 @@ dlrm_status pack_update(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* 
     memset(&a, 0, sizeof a);
     int64_t base = 0;
     for (int i = 0; i < tables->num_tables; ++i) {
-        if (upd->rule == DLRM_RULE_ADAGRAD) {
-            if (upd->accum[i] == nullptr || !aligned16(upd->accum[i])) return DLRM_ERR_INVALID_ARG;
-            a.accum[i] = upd->accum[i];
-        }
         a.tables[i] = static_cast<float*>(tables->data[i]);
         a.num_rows[i] = tables->num_rows[i];
         a.row_base[i] = base;
@@ -233,23 +221,41 @@ dlrm_status pack_update(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* 
     a.B = bags->batch;
     a.nnz = bags->nnz;
     a.T = tables->num_tables;
-    a.mean = mode == DLRM_POOL_MEAN;
-    a.lr = upd->lr;
-    a.eps = upd->eps;
-    a.rule = upd->rule;
     a.t_magic = a.T >= 2 ? ~uint64_t{0} / static_cast<uint64_t>(a.T) + 1 : 0;
     return DLRM_OK;
 }
 
-}  // namespace
+// Checks shared by the row-update entry points; fills everything of the
+// parameter block but the interaction inputs.
+dlrm_status pack_update(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                        const dlrm_update* upd, void* workspace, int32_t* status_dev)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (tables->dtype != DLRM_F32) return DLRM_ERR_UNSUPPORTED;
+    if (!mode_ok(mode) || upd == nullptr || workspace == nullptr || !aligned16(workspace)) return DLRM_ERR_INVALID_ARG;
+    if (upd->rule != DLRM_RULE_ADAGRAD && upd->rule != DLRM_RULE_SGD) return DLRM_ERR_INVALID_ARG;
+    if (upd->rule == DLRM_RULE_ADAGRAD && upd->accum == nullptr) return DLRM_ERR_INVALID_ARG;
+    if ((st = pack_rows(a, tables, bags, status_dev)) != DLRM_OK) return st;
+    for (int i = 0; i < tables->num_tables; ++i) {
+        if (upd->rule == DLRM_RULE_ADAGRAD) {
+            if (upd->accum[i] == nullptr || !aligned16(upd->accum[i])) return DLRM_ERR_INVALID_ARG;
+            a.accum[i] = upd->accum[i];
+        }
+    }
+    a.mean = mode == DLRM_POOL_MEAN;
+    a.lr = upd->lr;
+    a.eps = upd->eps;
+    a.rule = upd->rule;
+    return DLRM_OK;
+}
 
-extern "C" {
-
-dlrm_status dlrm_sparse_bwd_update(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
-                                   const float* dense, const float* pooled_saved, const float* grad_out,
-                                   float* grad_dense, const dlrm_update* update, void* workspace,
-                                   size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
-                                   cudaStream_t side_stream)
+// The training step; presorted: the workspace holds the sorted lookups of these bags (dlrm_sparse_bwd_sort).
+dlrm_status sparse_bwd(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode, const float* dense,
+                       const float* pooled_saved, const float* grad_out, float* grad_dense, const dlrm_update* update,
+                       void* workspace, size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
+                       cudaStream_t side_stream, bool presorted, cudaEvent_t sorted)
 {
     BwdArgs a;
     dlrm_status st = pack_update(a, tables, bags, mode, update, workspace, status_dev);
@@ -267,7 +273,47 @@ dlrm_status dlrm_sparse_bwd_update(const dlrm_tables* tables, const dlrm_bags* b
     a.grad_out = grad_out;
     a.grad_dense = grad_dense;
     return dlrm::launch_backward(a, tables->dim, bags->index_type, dlrm::kFromInteraction, nullptr, workspace,
-                                 workspace_bytes, stream, side_stream);
+                                 workspace_bytes, stream, side_stream, presorted, sorted);
+}
+
+}  // namespace
+
+extern "C" {
+
+dlrm_status dlrm_sparse_bwd_update(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                   const float* dense, const float* pooled_saved, const float* grad_out,
+                                   float* grad_dense, const dlrm_update* update, void* workspace,
+                                   size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
+                                   cudaStream_t side_stream)
+{
+    return sparse_bwd(tables, bags, mode, dense, pooled_saved, grad_out, grad_dense, update, workspace,
+                      workspace_bytes, status_dev, stream, side_stream, false, nullptr);
+}
+
+dlrm_status dlrm_sparse_bwd_sort(const dlrm_tables* tables, const dlrm_bags* bags, void* workspace,
+                                 size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream)
+{
+    dlrm_status st = check_tables(tables);
+    if (st != DLRM_OK) return st;
+    if ((st = check_bags(bags, tables->num_tables)) != DLRM_OK) return st;
+    if (tables->dtype != DLRM_F32) return DLRM_ERR_UNSUPPORTED;
+    if (workspace == nullptr || !aligned16(workspace)) return DLRM_ERR_INVALID_ARG;
+    BwdArgs a;
+    if ((st = pack_rows(a, tables, bags, status_dev)) != DLRM_OK) return st;
+    if (workspace_bytes < dlrm::bwd_workspace_bytes(bags->batch, tables->num_tables, tables->dim, bags->nnz,
+                                                    dlrm::kFromInteraction, true))
+        return DLRM_ERR_INVALID_ARG;
+    return dlrm::launch_sort(a, tables->dim, bags->index_type, workspace, workspace_bytes, stream);
+}
+
+dlrm_status dlrm_sparse_bwd_update_sorted(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,
+                                          const float* dense, const float* pooled_saved, const float* grad_out,
+                                          float* grad_dense, const dlrm_update* update, void* workspace,
+                                          size_t workspace_bytes, int32_t* status_dev, cudaEvent_t sorted,
+                                          cudaStream_t stream)
+{
+    return sparse_bwd(tables, bags, mode, dense, pooled_saved, grad_out, grad_dense, update, workspace,
+                      workspace_bytes, status_dev, stream, nullptr, true, sorted);
 }
 
 dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,

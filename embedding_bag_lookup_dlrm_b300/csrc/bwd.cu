@@ -925,6 +925,16 @@ dlrm_status launch_interact_bwd(const BwdArgs& a, float* dP, cudaStream_t s)
     return cudaGetLastError() == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA;
 }
 
+// Key bits: valid keys are < total rows, so the sentinel's low bits sort after them; the passes split
+// them into digits of at most kMaxRadixBits bits.  The sorted pairs end in ping-pong buffer passes % 2.
+void radix_digits(const BwdArgs& a, int* passes, int* dbits)
+{
+    int bits = 1;
+    while ((int64_t{1} << bits) <= a.row_base[a.T]) ++bits;
+    *passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
+    *dbits = (bits + *passes - 1) / *passes;
+}
+
 // Keys, then the stable radix sort, on stream ks; returns the ping-pong buffer holding the sorted pairs.
 template <typename TI>
 dlrm_status sort_keys(const BwdArgs& a, const Workspace& w, cudaStream_t ks, int* sorted)
@@ -935,12 +945,8 @@ dlrm_status sort_keys(const BwdArgs& a, const Workspace& w, cudaStream_t ks, int
     expand_keys_kernel<TI><<<static_cast<unsigned>(expand_blocks < 148 * 64 ? expand_blocks : 148 * 64), 256, 0, ks>>>(
         a, w.keys[0], w.vals[0]);
 
-    // key bits: valid keys are < total rows, so the sentinel's low bits sort after them; the passes
-    // split them into digits of at most kMaxRadixBits bits
-    int bits = 1;
-    while ((int64_t{1} << bits) <= a.row_base[a.T]) ++bits;
-    const int passes = (bits + kMaxRadixBits - 1) / kMaxRadixBits;
-    const int dbits = (bits + passes - 1) / passes;
+    int passes = 0, dbits = 0;
+    radix_digits(a, &passes, &dbits);
     // set on every call: the attribute belongs to the current device's context
     if (cudaFuncSetAttribute(radix_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(ScatterSmem))) != cudaSuccess)
@@ -989,12 +995,14 @@ dlrm_status launch_interact_bwd_groups(const BwdArgs& a, float* dP, cudaStream_t
 
 // The training step (source kFromInteraction: dP from the interaction backward, already divided by the
 // bag lengths in mean mode) or the row update from a given pooled gradient (kFromPooledGrad).
+// presorted: the workspace holds the sorted pairs of these bags (sort_keys queued earlier by the caller),
+// so only the dP rows and the per-row sums run here; the per-row sums wait for `sorted` when it is given.
 template <int D, typename TI>
 dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const float* grad_pooled, cudaStream_t s,
-                         cudaStream_t side)
+                         cudaStream_t side, bool presorted, cudaEvent_t sorted)
 {
     Fork f;
-    const bool two = side != nullptr && side != s && a.nnz > 0;
+    const bool two = !presorted && side != nullptr && side != s && a.nnz > 0;
     if (two && (cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
                 cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess ||
                 cudaEventRecord(f.fork, s) != cudaSuccess || cudaStreamWaitEvent(side, f.fork, 0) != cudaSuccess))
@@ -1002,7 +1010,14 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const
     const cudaStream_t ks = two ? side : s;
 
     int cur = 0;
-    dlrm_status st = a.nnz > 0 ? sort_keys<TI>(a, w, ks, &cur) : DLRM_OK;
+    dlrm_status st = DLRM_OK;
+    if (presorted) {
+        int passes = 0, dbits = 0;
+        radix_digits(a, &passes, &dbits);
+        cur = passes & 1;
+    } else if (a.nnz > 0) {
+        st = sort_keys<TI>(a, w, ks, &cur);
+    }
     // beside the sort: the dP rows the per-row sums read
     const float* dP = source == kFromInteraction ? w.dP : grad_pooled;
     if (st == DLRM_OK) {
@@ -1021,6 +1036,7 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const
     if (two && (cudaEventRecord(f.join, side) != cudaSuccess || cudaStreamWaitEvent(s, f.join, 0) != cudaSuccess))
         return DLRM_ERR_CUDA;
     if (st != DLRM_OK || a.nnz == 0) return st;
+    if (presorted && sorted != nullptr && cudaStreamWaitEvent(s, sorted, 0) != cudaSuccess) return DLRM_ERR_CUDA;
 
     const unsigned seg_blocks = static_cast<unsigned>((w.num_chunks + kSegThreads / kWarp - 1) / (kSegThreads / kWarp));
     constexpr size_t seg_smem = seg_smem_bytes<D>();
@@ -1036,10 +1052,10 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const
 
 template <int D>
 dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, int source, const float* grad_pooled,
-                         cudaStream_t s, cudaStream_t side)
+                         cudaStream_t s, cudaStream_t side, bool presorted, cudaEvent_t sorted)
 {
-    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, source, grad_pooled, s, side)
-                                  : run_backward<D, int64_t>(a, w, source, grad_pooled, s, side);
+    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, source, grad_pooled, s, side, presorted, sorted)
+                                  : run_backward<D, int64_t>(a, w, source, grad_pooled, s, side, presorted, sorted);
 }
 
 bool with_dP(int source, bool mean) { return source == kFromInteraction || mean; }
@@ -1054,19 +1070,32 @@ size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz, int sou
 }
 
 dlrm_status launch_backward(const BwdArgs& a, int dim, int index_type, int source, const float* grad_pooled,
-                            void* workspace, size_t workspace_bytes, cudaStream_t s, cudaStream_t side)
+                            void* workspace, size_t workspace_bytes, cudaStream_t s, cudaStream_t side, bool presorted,
+                            cudaEvent_t sorted)
 {
     size_t need = 0;
     const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, with_dP(source, a.mean != 0), &need);
     if (workspace_bytes < need) return DLRM_ERR_INVALID_ARG;
     switch (dim) {
-        case 16: return dispatch_bwd<16>(a, index_type, w, source, grad_pooled, s, side);
-        case 32: return dispatch_bwd<32>(a, index_type, w, source, grad_pooled, s, side);
-        case 64: return dispatch_bwd<64>(a, index_type, w, source, grad_pooled, s, side);
-        case 128: return dispatch_bwd<128>(a, index_type, w, source, grad_pooled, s, side);
-        case 256: return dispatch_bwd<256>(a, index_type, w, source, grad_pooled, s, side);
+        case 16: return dispatch_bwd<16>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
+        case 32: return dispatch_bwd<32>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
+        case 64: return dispatch_bwd<64>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
+        case 128: return dispatch_bwd<128>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
+        case 256: return dispatch_bwd<256>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
         default: return DLRM_ERR_UNSUPPORTED;
     }
+}
+
+dlrm_status launch_sort(const BwdArgs& a, int dim, int index_type, void* workspace, size_t workspace_bytes,
+                        cudaStream_t s)
+{
+    if (dim != 16 && dim != 32 && dim != 64 && dim != 128 && dim != 256) return DLRM_ERR_UNSUPPORTED;
+    size_t need = 0;
+    const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, with_dP(kFromInteraction, a.mean != 0), &need);
+    if (workspace_bytes < need) return DLRM_ERR_INVALID_ARG;
+    if (a.nnz == 0) return DLRM_OK;
+    int cur = 0;
+    return index_type == DLRM_I32 ? sort_keys<int32_t>(a, w, s, &cur) : sort_keys<int64_t>(a, w, s, &cur);
 }
 
 dlrm_status launch_interact_backward(const BwdArgs& a, int dim, float* grad_pooled, cudaStream_t s)

@@ -89,8 +89,16 @@ size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz, int sou
 
 // side: a second stream for the key build and sort (nullptr or == stream: one stream).
 // grad_pooled: the source of kFromPooledGrad (ignored otherwise).
+// presorted: the workspace holds the sorted lookups of these bags from launch_sort (side is then unused);
+// sorted, if given, is an event the per-row sums wait for (the interaction backward does not).
 dlrm_status launch_backward(const BwdArgs& args, int dim, int index_type, int source, const float* grad_pooled,
-                            void* workspace, size_t workspace_bytes, cudaStream_t stream, cudaStream_t side);
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream, cudaStream_t side,
+                            bool presorted = false, cudaEvent_t sorted = nullptr);
+
+// The lookup keys of the bags and their stable radix sort into a training-step workspace (the layout
+// launch_backward with source kFromInteraction reads), on `stream`.
+dlrm_status launch_sort(const BwdArgs& args, int dim, int index_type, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
 
 // The interaction backward alone: grad_dense and grad_pooled (not scaled by bag lengths).
 dlrm_status launch_interact_backward(const BwdArgs& args, int dim, float* grad_pooled, cudaStream_t stream);

@@ -103,6 +103,34 @@ def test_backward_rejects_batches_past_32_bit_sort_fields(lib):
     assert n.value > 1 << 36
 
 
+def test_split_step_host_checks(lib):
+    """dlrm_sparse_bwd_sort and dlrm_sparse_bwd_update_sorted refuse on the host what the one-call step
+    refuses: past the 32-bit sort fields, bf16 tables, no or misaligned workspace, a workspace too small."""
+    def sort_status(T, B, nnz, rows=10, dtype=0, ws=0x10, ws_bytes=1 << 62):
+        tb, _p, _r = _tables(T=T, D=16, rows=rows, dtype=dtype)
+        bags = dl.DlrmBags(B, nnz, 1, 0x2000, 0x3000)
+        return lib.dlrm_sparse_bwd_sort(ctypes.byref(tb), ctypes.byref(bags), ws, ws_bytes, None, None)
+
+    assert sort_status(T=2, B=1 << 31, nnz=8) == dl.DLRM_ERR_UNSUPPORTED       # T*B = 2^32
+    assert sort_status(T=2, B=4, nnz=1 << 32) == dl.DLRM_ERR_UNSUPPORTED       # nnz = 2^32
+    assert sort_status(T=1, B=4, nnz=8, rows=(1 << 32) - 1) == dl.DLRM_ERR_UNSUPPORTED
+    assert sort_status(T=2, B=4, nnz=8, dtype=1) == dl.DLRM_ERR_UNSUPPORTED     # bf16 tables
+    assert sort_status(T=2, B=4, nnz=8, ws=None) == dl.DLRM_ERR_INVALID_ARG
+    assert sort_status(T=2, B=4, nnz=8, ws=0x18) == dl.DLRM_ERR_INVALID_ARG     # not 16-byte aligned
+    assert sort_status(T=2, B=4, nnz=8, ws_bytes=64) == dl.DLRM_ERR_INVALID_ARG  # too small
+
+    tb, _p, _r = _tables(T=2, D=16)
+    bags = dl.DlrmBags(4, 1 << 32, 1, 0x2000, 0x3000)
+    acc = (ctypes.c_void_p * 2)(0x10, 0x10)
+    upd = dl.DlrmUpdate(0, 0.01, 1e-8, ctypes.cast(acc, ctypes.POINTER(ctypes.c_void_p)))
+    args = (ctypes.byref(tb), ctypes.byref(bags), 0, 0x10, 0x10, 0x10, 0x10, ctypes.byref(upd), 0x10, 1 << 62,
+            None, None, None)
+    assert lib.dlrm_sparse_bwd_update_sorted(*args) == dl.DLRM_ERR_UNSUPPORTED  # nnz = 2^32
+    bags.nnz = 8
+    upd.rule = 9
+    assert lib.dlrm_sparse_bwd_update_sorted(*args) == dl.DLRM_ERR_INVALID_ARG  # unknown rule
+
+
 def test_static_scratch_size_matches_header(lib):
     """The binding's copy of DLRM_STATIC_SCRATCH_BYTES is the header's."""
     text = open(os.path.join(ROOT, "include", "dlrm_sparse.h")).read()

@@ -127,6 +127,56 @@ def test_bwd_bitwise_reproducible():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("mode,itype,rule,V,wait", [("sum", "i32", "adagrad", 400, "event"),
+                                                    ("mean", "i64", "sgd", 3000, "stream"),
+                                                    ("sum", "i64", "adagrad", 1 << 17, "event")])
+def test_sort_beside_forward_matches_one_call(mode, itype, rule, V, wait):
+    """dlrm_sparse_bwd_sort on a second stream while the forward runs, then dlrm_sparse_bwd_update_sorted
+    (waiting for the sort through its event argument, or through the caller's stream wait): tables,
+    accumulators and grad_dense bit for bit those of the one-call step (dlrm_sparse_bwd_update), over two
+    consecutive steps (the second one's sort overwrites the first one's pairs).  V = 2^17 rows per table
+    (3.4 M rows in all) makes 22 key bits: three radix passes, against two for the smaller tables."""
+    B, T, D = 3000, 26, 128
+    tabs, Vs, idx, off, dense = random_case(41, B, T, D, V, 0, 8, value_scale=0.05)
+    rng = np.random.default_rng(5)
+    g = [torch.from_numpy(rng.standard_normal((B, D + 27 * 13)).astype(np.float32)).cuda() for _ in range(2)]
+    di, do, dx = dev_index(idx, itype), dev_index(off, itype), torch.from_numpy(dense).cuda()
+    results = []
+    for split in (False, True):
+        dt = dev_tables(tabs, "f32")
+        acc = [torch.full((v,), 0.1, device="cuda") for v in Vs] if rule == "adagrad" else None
+        ws = torch.empty(dl.dlrm_sparse_bwd_workspace_size(dt, di, do), dtype=torch.uint8, device="cuda")
+        ws.fill_(0xA5)
+        ps = torch.empty((B, T, D), device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        main, side = torch.cuda.Stream(), torch.cuda.Stream()
+        gds = []
+        with torch.cuda.stream(main):
+            for k in range(2):
+                if split:
+                    fork, join = torch.cuda.Event(), torch.cuda.Event()
+                    fork.record(main)
+                    side.wait_event(fork)
+                    dl.dlrm_sparse_bwd_sort(dt, di, do, ws, status=status, stream=side)
+                    join.record(side)
+                    dl.dlrm_sparse_fwd(dt, di, do, dx, mode, pooled_save=ps, status=status, stream=main)
+                    if wait == "stream":
+                        main.wait_event(join)
+                    gd = dl.dlrm_sparse_bwd_update_sorted(dt, di, do, dx, ps, g[k], rule, 0.01, 1e-8, acc, mode,
+                                                          workspace=ws, status=status,
+                                                          sorted=join if wait == "event" else None, stream=main)
+                else:
+                    dl.dlrm_sparse_fwd(dt, di, do, dx, mode, pooled_save=ps, status=status, stream=main)
+                    gd = dl.dlrm_sparse_bwd_update(dt, di, do, dx, ps, g[k], rule, 0.01, 1e-8, acc, mode,
+                                                   workspace=ws, status=status, stream=main)
+                gds.append(gd.clone())
+        torch.cuda.synchronize()
+        assert status.item() == 0, dl.status_string(status.item())
+        results.append([torch.cat([t.flatten() for t in dt])] + ([torch.cat(acc)] if acc else []) + gds)
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
+
+
 def test_bwd_flags_bad_index(orc):
     B, T, D, V = 50, 3, 64, 30
     tabs, Vs, idx, off, dense = random_case(41, B, T, D, V, 1, 3, value_scale=0.05)

@@ -86,11 +86,12 @@ def test_head_bce(M, K):
     assert abs((bt.item() - b[0]) - (-0.1 * db)) <= 1e-5
 
 
-@pytest.mark.parametrize("B,mode", [(1500, "sum"), (3000, "mean")])
-def test_dlrm_training_step(B, mode):
+@pytest.mark.parametrize("B,mode,side", [(1500, "sum", False), (3000, "mean", True)])
+def test_dlrm_training_step(B, mode, side):
     """The whole step: bottom 13 -> 64 -> 128, T = 26 tables (D = 128, bags 1..8), top 479 -> 256 -> 64,
     head 64 -> 1.  Loss, the interaction output, every MLP weight after SGD and every table row after
-    row-wise Adagrad against the oracle."""
+    row-wise Adagrad against the oracle; with `side`, the sparse backward's sort runs on a second stream
+    beside the forward."""
     orc = oracle.get()
     T, D, V = 26, 128, 400
     rng = np.random.default_rng(B)
@@ -113,7 +114,8 @@ def test_dlrm_training_step(B, mode):
                          [(cuda(w), cuda(b)) for w, b in top], (cuda(head[0]), cuda(np.array([head[1]]))))
     acc = [torch.full((v,), 0.1, device="cuda") for v in Vs]
     loss, prob = model.train_step(cuda(dense_in), dev_index(idx, "i32"), dev_index(off, "i32"), cuda(label), lr_mlp,
-                                  lr_emb, 1e-8, acc, mode=mode)
+                                  lr_emb, 1e-8, acc, mode=mode,
+                                  side_stream=torch.cuda.Stream() if side else None)
     torch.cuda.synchronize()
     assert abs(loss.item() - ref["loss"]) <= 1e-4 * max(1.0, ref["loss"])
     # x (the bottom MLP's output) against its layer's scale |h| |W|^T + |b|
