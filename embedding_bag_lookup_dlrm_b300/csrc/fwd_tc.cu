@@ -37,7 +37,10 @@
 // Epilogue.  Each warp loads its rows of its sample's diagonal block from TMEM
 // (thread i gets row i of the Gram), scatters the values above the diagonal
 // into the staged output row, and the CTA stores the tile's output rows with
-// coalesced stores.
+// coalesced stores.  A one-sample tile (N > 64: a triangle of up to 8,001
+// values) instead leaves through one bulk copy of the TMA engine, issued by
+// one thread, while the warps go on to the next tile; its x went straight to
+// out when it was split.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -54,6 +57,10 @@ constexpr int kMaxCtasPerSm = 4;    // 4 x 128 TMEM columns fill the SM's 512
 constexpr int kMinSmemPerCta = 48 * 1024;  // keeps at most 4 CTAs on an SM
 constexpr uint32_t kFull = 0xffffffffu;
 
+// Floats between the staged triangles of a tile's samples: room for W - D values placed at the 16-byte
+// residue of their place in out (up to 3 floats in), each slot 16-byte aligned.
+__host__ __device__ constexpr int stage_stride(int D, int W) { return (W - D + 3 + 3) & ~3; }
+
 // Shared memory of one CTA, byte offsets from a 1024-byte aligned base.
 struct TcLayout {
     int hi, lo, stage, tables, bar, tmem_slot, bytes;
@@ -67,8 +74,8 @@ __host__ __device__ inline TcLayout make_tc_layout(int D, int S, int W)
     const int operand = kTileRows * D * 2;  // one bf16 operand
     l.hi = 0;
     l.lo = operand;
-    l.stage = 2 * operand;                  // S output rows of W floats
-    l.tables = l.stage + round_up(S * W * 4, 16);  // table addresses and row counts
+    l.stage = 2 * operand;  // S output rows of W floats; one-sample tiles: the triangle alone (stage_stride)
+    l.tables = l.stage + (S == 1 ? stage_stride(D, W) * 4 : round_up(S * W * 4, 16));  // table addresses, rows
     l.bar = l.tables + 16 * kMaxTablesTc;
     l.tmem_slot = l.bar + 8;  // after the MMA barrier
     l.bytes = l.tmem_slot + 16;
@@ -180,6 +187,21 @@ __device__ __forceinline__ void store_split4(unsigned char* hi, unsigned char* l
     *reinterpret_cast<uint2*>(lo + off) = make_uint2(bf2_bits(l01), bf2_bits(l23));
 }
 
+// Shared -> global through the TMA engine (both addresses 16-byte aligned, bytes a multiple of 16), one
+// bulk async-group per commit; the issuing thread waits for the group's reads of shared memory (.read)
+// before the buffer is written again, and for its completion before the CTA exits.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src_smem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src_smem)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_done() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy writes to shared memory made visible to a later bulk copy's reads (each writing thread).
+__device__ __forceinline__ void fence_smem_for_bulk() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // 16 bytes global -> shared through the async-copy path (cached in L2 only).
 __device__ __forceinline__ void cp_async16(void* dst, const void* src)
 {
@@ -262,8 +284,8 @@ __device__ __forceinline__ void finish_row(const FwdArgs& a, unsigned char* op_h
     constexpr int S = kTileRows / NP;
     const int rt = kWarp * warp + rr;
     const int k = rt % NP;
-    if (k == 0) {
-        float* dst = stage + (rt / NP) * W + lane * C;
+    if (k == 0) {  // x, exactly: straight to its output row in one-sample tiles, else to the staged row
+        float* dst = S == 1 ? a.out + tile * W + lane * C : stage + (rt / NP) * W + lane * C;
 #pragma unroll
         for (int c = 0; c < C; ++c) dst[c] = v[c];
     } else if (MODE == kFused && a.pooled_out != nullptr) {
@@ -311,6 +333,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && !MULTI) ? 4 : 3) forward
     constexpr uint32_t F32_BYTES = D * 4;
     constexpr uint32_t TE_BYTES = D * sizeof(TE);
     using SliceT = Slice<SLICE>;
+    // One-sample tiles store the output triangle through the TMA engine (a bulk copy from shared memory);
+    // tiles of several short rows copy them out with coalesced stores of every thread.
+    constexpr bool kBulkOut = S == 1;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -658,8 +683,8 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && !MULTI) ? 4 : 3) forward
                             v[q] = make_float4(__fdiv_rn(v[q].x, fl), __fdiv_rn(v[q].y, fl), __fdiv_rn(v[q].z, fl),
                                                __fdiv_rn(v[q].w, fl));
                         }
-                        if (q0 + q == 0 && g32 == 0 && x_warp) {  // x, exactly (output rows are W floats apart)
-                            float* dst = stage + (row / NP) * W + c32 * 4;
+                        if (q0 + q == 0 && g32 == 0 && x_warp) {  // x, exactly (see the output stores)
+                            float* dst = kBulkOut ? a.out + tile * W + c32 * 4 : stage + (row / NP) * W + c32 * 4;
                             dst[0] = v[q].x;
                             dst[1] = v[q].y;
                             dst[2] = v[q].z;
@@ -712,6 +737,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && !MULTI) ? 4 : 3) forward
                 tc::mma_bf16(tmem, tc::desc_kmajor_sw128(A), tc::desc_kmajor_sw128(B), idesc, it != 0);
             }
             tc::commit(mma_bar);
+            if constexpr (kBulkOut) bulk_wait_read();  // the last tile's output stores have read the staging area
         }
         mma_pending = true;
         m = m_next;
@@ -734,7 +760,10 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && !MULTI) ? 4 : 3) forward
             const int i = i0 + lane;
             const int64_t bw = tile * S + sw;
             if (bw < a.B && i0 < N) {
-                float* st = stage + sw * W;
+                // one-sample tiles: the triangle starts at the same 16-byte residue as its place in out
+                const int sh =
+                    kBulkOut ? static_cast<int>((reinterpret_cast<uintptr_t>(a.out + bw * W + D) >> 2) & 3u) : 0;
+                float* st = kBulkOut ? stage + sh - D : stage + sw * W;
                 const int base_i = D + i * N - i * (i + 1) / 2 - i - 1;  // out position of (i, j) is base_i + j
                 for (int cb = i0 / kWarp; cb * kWarp < N; ++cb) {
                     uint32_t z[32];
@@ -750,19 +779,43 @@ __global__ void __launch_bounds__(kThreads, (D == 64 && !MULTI) ? 4 : 3) forward
                 }
             }
         }
+        if constexpr (kBulkOut) fence_smem_for_bulk();  // the staged triangle, written by every thread, to the TMA engine
         tc::fence_before_sync();
         __syncthreads();
 
-        // ---- the tile's output rows, coalesced ----
-        {
+        if constexpr (kBulkOut) {
+            // ---- one-sample tile (a long triangle): its 16-byte aligned body by one bulk copy from thread 0,
+            //      which also waits for it; a head and a tail of at most 3 floats by plain stores (x went out
+            //      in the split) ----
+            if (tile < a.B) {
+                const int Wt = W - D;
+                float* o = a.out + tile * W + D;
+                const int sh = static_cast<int>((reinterpret_cast<uintptr_t>(o) >> 2) & 3u);
+                const int head = min((4 - sh) & 3, Wt);
+                const int body = (Wt - head) & ~3;
+                const float* st = stage + sh;
+                if (threadIdx.x == 0) {
+                    if (body > 0) bulk_s2g(o + head, st + head, static_cast<uint32_t>(body) * 4u);
+                    bulk_commit();
+                } else if (warp == 1 && lane < 6) {  // lanes 0..2: the head, 3..5: the tail
+                    const int t = head + body + (lane - 3);
+                    if (lane < 3 && lane < head) o[lane] = st[lane];
+                    if (lane >= 3 && t < Wt) o[t] = st[t];
+                }
+            }
+        } else {
+            // ---- the tile's output rows, coalesced ----
             const int64_t b0 = tile * S;
             const int ns = static_cast<int>(min(static_cast<int64_t>(S), a.B - b0));
             float* o = a.out + b0 * W;
             for (int e = threadIdx.x; e < ns * W; e += kThreads) o[e] = stage[e];
         }
-        __syncthreads();  // staging and operands free for the next tile
+        __syncthreads();  // operands free for the next tile (the staging area once the bulk reads are done)
     }
 
+    if constexpr (kBulkOut) {
+        if (threadIdx.x == 0) bulk_wait_done();  // the output stores are complete before the CTA exits
+    }
     if (timed_out) {
         if (threadIdx.x == 0) flag_status(a.status, DLRM_ERR_TIMEOUT);
         // let copies and an MMA still in flight finish (bounded) before shared memory and TMEM are released
