@@ -68,6 +68,13 @@ static int host_checks(void)
         CHECK(dlrm_embbag_bwd_update(&tb, &bags, DLRM_POOL_SUM, (const float *)0x10, &upd,
                                      (void *)0x10, (size_t)1 << 62, NULL, 0, 0) ==
               DLRM_ERR_INVALID_ARG);
+        /* the split training step: a workspace too small for the sort, an unknown rule */
+        bags.index_type = DLRM_I32;
+        CHECK(dlrm_sparse_bwd_sort(&tb, &bags, (void *)0x10, 64, NULL, 0) == DLRM_ERR_INVALID_ARG);
+        CHECK(dlrm_sparse_bwd_update_sorted(&tb, &bags, DLRM_POOL_SUM, (const float *)0x10,
+                                            (const float *)0x10, (const float *)0x10, (float *)0x10,
+                                            &upd, (void *)0x10, (size_t)1 << 62, NULL,
+                                            (cudaEvent_t)0, 0) == DLRM_ERR_INVALID_ARG);
     }
     {
         int32_t shard[2] = {0, 0}, slot[2] = {0, 0}; /* slot 0 twice: inconsistent */
