@@ -140,6 +140,37 @@ def test_onehot_fp32_bit_exact(orc):
     assert np.array_equal(ps.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("D,T,B,Lmax", [(64, 100, 301, 1), (128, 80, 203, 3), (128, 26, 401, 1), (64, 40, 150, 2)])
+def test_out_at_every_4_byte_offset(D, T, B, Lmax):
+    """`out` need only be 4-byte aligned.  Rows written at 1, 2 and 3 floats past a 16-byte boundary (the
+    one-sample tiles of N > 64 send their triangle by a bulk copy whose body must start on a 16-byte
+    boundary of out, with plain stores for a head and a tail) equal the rows written to an aligned buffer
+    bit for bit, for the fused forward and the interaction-only call; the floats around the rows stay
+    untouched."""
+    tabs, Vs, idx, off, dense = random_case(900 + T, B, T, D, 700, 1, Lmax, value_scale=0.1)
+    dt, di, do = dev_tables(tabs, "f32"), dev_index(idx, "i32"), dev_index(off, "i32")
+    dx = torch.from_numpy(dense).cuda()
+    N = T + 1
+    W = D + N * (N - 1) // 2
+    ref = dl.dlrm_sparse_fwd(dt, di, do, dx)
+    pooled = torch.empty((B, T, D), device="cuda")
+    dl.dlrm_embbag_fwd(dt, di, do, pooled=pooled)
+    ref_i = torch.empty((B, W), device="cuda")
+    dl.dlrm_interact_fwd(dx, pooled, out=ref_i)
+    for shift in (1, 2, 3):
+        for call in ("fused", "interact"):
+            buf = torch.full((B * W + 8,), -7.0, device="cuda")
+            out = buf[shift:shift + B * W].view(B, W)
+            if call == "fused":
+                dl.dlrm_sparse_fwd(dt, di, do, dx, out=out)
+            else:
+                dl.dlrm_interact_fwd(dx, pooled, out=out)
+            torch.cuda.synchronize()
+            want = ref if call == "fused" else ref_i
+            assert torch.equal(out.view(torch.int32), want.view(torch.int32)), (call, shift)
+            assert torch.all(buf[:shift] == -7.0) and torch.all(buf[shift + B * W:] == -7.0), (call, shift)
+
+
 def _round_to_16_bits(x):
     """x rounded to 16 significant bits: the sum of two bfloat16 values, which
     is what the tensor-core Gram carries of each fp32 operand."""
