@@ -674,9 +674,7 @@ def run_ours(args, w):
     roof = {"bound": "hbm", "achieved": phases[dom]["gbs"], "peak": peak, "unit": "GB/s",
             "frac": phases[dom]["frac"], "traffic": traffic_for(args.workload) if phase_is_traced(args, dom) else None,
             "kernel": kernel_of_phase(args, w, dom), "phase": dom, "peak_source": f"{src} (hbm_gbs, burst copy)",
-            **({"traffic_capped_tables": {k: traffic_record(args.workload)[k] for k in
-                                          ("small_case", "small_case_uniform", "why_null")
-                                          if k in traffic_record(args.workload)}}
+            **({"traffic_capped_tables": capped_traffic(traffic_record(args.workload))}
                if phase_is_traced(args, dom) and traffic_record(args.workload) else {}),
             "algorithmic_bytes_per_launch": phases[dom]["bytes"], "frac_of_nominal_8000":
             round(phases[dom]["gbs"] / 8000.0, 4), "median_launch_ms": round(statistics.median(phase_ms[dom]), 4),
@@ -752,8 +750,22 @@ def launches_per_step(args, w, plan=None) -> int:
 
 
 def phase_is_traced(args, phase) -> bool:
-    """profiles/traffic.json holds DRAM bytes of the plain forward kernel."""
-    return args.shards == 1 and not args.uniform and args.max_rows == 0 and phase == "forward"
+    """profiles/traffic.json holds DRAM bytes of the plain forward kernel (capped tables, Zipf and uniform)."""
+    return args.shards == 1 and args.max_rows == 0 and phase == "forward"
+
+
+def capped_traffic(rec: dict) -> dict:
+    """The capped-table captures of a traffic record, each with its DRAM GB/s (read + write over the
+    captured launch's duration) beside its L2 hit rate."""
+    out = {}
+    for k in ("small_case", "small_case_uniform"):
+        if k in rec:
+            c = dict(rec[k])
+            c["dram_gbs"] = round((c["dram_read_bytes"] + c["dram_write_bytes"]) / (c["duration_us"] * 1e3), 1)
+            out[k] = c
+    if "why_null" in rec:
+        out["why_null"] = rec["why_null"]
+    return out
 
 
 def kernel_of_phase(args, w, phase) -> str:
