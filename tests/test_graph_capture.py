@@ -1,8 +1,9 @@
-"""A training step (dlrm_sparse_fwd with pooled_save, then dlrm_sparse_bwd_adagrad)
-captured into a CUDA graph and replayed gives, bitwise, what the same steps give
-when called directly: the caller's side stream forks from and joins the
-captured stream (through events the call makes and releases), and every kernel
-of the step is deterministic.  Steps queued on independent streams at once give
+"""A training step (dlrm_sparse_fwd with pooled_save, then dlrm_sparse_bwd_adagrad,
+or the split step: dlrm_sparse_bwd_sort beside the forward, then
+dlrm_sparse_bwd_update_sorted) captured into a CUDA graph and replayed gives,
+bitwise, what the same steps give when called directly: the caller's side
+stream forks from and joins the captured stream (through events), and every
+kernel of the step is deterministic.  Steps queued on independent streams at once give
 the results of the same steps run one after another: the library holds no
 state shared between calls."""
 import numpy as np
@@ -18,9 +19,9 @@ pytestmark = pytest.mark.gpu
 class Step:
     """Buffers of one training step, allocated once, so that a graph can replay it."""
 
-    def __init__(self, tabs, Vs, idx, off, dense, grad_out, D, side=None):
+    def __init__(self, tabs, Vs, idx, off, dense, grad_out, D, side=None, split=False):
         B, T = dense.shape[0], len(tabs)
-        self.side = side
+        self.side, self.split = side, split
         self.tables = dev_tables(tabs, "f32")
         self.accum = [torch.full((v,), 0.1, device="cuda") for v in Vs]
         self.di, self.do = dev_index(idx, "i32"), dev_index(off, "i32")
@@ -34,6 +35,19 @@ class Step:
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
 
     def run(self):
+        if self.split:  # the sort on the side stream beside the forward; the per-row sums wait for its event
+            cur = torch.cuda.current_stream()
+            fork, sorted_ev = torch.cuda.Event(), torch.cuda.Event()
+            fork.record(cur)
+            self.side.wait_event(fork)
+            dl.dlrm_sparse_bwd_sort(self.tables, self.di, self.do, self.ws, status=self.status, stream=self.side)
+            sorted_ev.record(self.side)
+            dl.dlrm_sparse_fwd(self.tables, self.di, self.do, self.dx, out=self.out, pooled_save=self.ps,
+                               status=self.status)
+            dl.dlrm_sparse_bwd_update_sorted(self.tables, self.di, self.do, self.dx, self.ps, self.g, "adagrad",
+                                             0.01, 1e-8, self.accum, grad_dense=self.gd, workspace=self.ws,
+                                             status=self.status, sorted=sorted_ev)
+            return
         dl.dlrm_sparse_fwd(self.tables, self.di, self.do, self.dx, out=self.out, pooled_save=self.ps,
                            status=self.status)
         dl.dlrm_sparse_bwd_adagrad(self.tables, self.accum, self.di, self.do, self.dx, self.ps, self.g, 0.01, 1e-8,
@@ -44,14 +58,17 @@ class Step:
                                                                                       self.gd.clone()]
 
 
-@pytest.mark.parametrize("two_streams", [True, False], ids=["side-stream", "one-stream"])
-def test_graph_replay_matches_direct_calls(two_streams):
+@pytest.mark.parametrize("layout", ["side-stream", "one-stream", "split"])
+def test_graph_replay_matches_direct_calls(layout):
+    """layout "split": dlrm_sparse_bwd_sort on the side stream beside the forward, then
+    dlrm_sparse_bwd_update_sorted waiting for the sort's event, captured the same way."""
     B, T, D, V = 3000, 26, 128, 500
     tabs, Vs, idx, off, dense = random_case(77, B, T, D, V, 1, 8, value_scale=0.05)
     g = np.random.default_rng(5).standard_normal((B, D + (T + 1) * T // 2)).astype(np.float32)
-    side = torch.cuda.Stream(priority=-100) if two_streams else None
+    side = torch.cuda.Stream(priority=-100) if layout != "one-stream" else None
+    split = layout == "split"
 
-    direct = Step(tabs, Vs, idx, off, dense, g, D, side)
+    direct = Step(tabs, Vs, idx, off, dense, g, D, side, split)
     direct.run()
     torch.cuda.synchronize()
     after_one = direct.state()
@@ -59,7 +76,7 @@ def test_graph_replay_matches_direct_calls(two_streams):
     torch.cuda.synchronize()
     after_two = direct.state()
 
-    graphed = Step(tabs, Vs, idx, off, dense, g, D, side)
+    graphed = Step(tabs, Vs, idx, off, dense, g, D, side, split)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         graphed.run()
