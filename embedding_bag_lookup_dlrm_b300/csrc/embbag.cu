@@ -155,12 +155,21 @@ __global__ void __launch_bounds__(kBagThreads) embbag_kernel(const __grid_consta
 // lane j resolves lookup j of the step (its bag by a 5-step search over the
 // lanes' list ends, its index by one load, coalesced where the bags' ranges
 // are contiguous) while the next step's indices are already on their way.
-// The warp then streams the step's rows, kRows in flight, each lane holding
+// The warp then streams the step's rows, a few at a time, each lane holding
 // 1/32 of a row (16, 8 or 4 bytes; D = 256 fp32: two 16-byte pieces), adding
 // each into the running bag's sum in lookup order; a finished bag is written
 // once.  One-hot batches thus keep 32 bags' rows moving per warp instead of
 // one.
-constexpr int kRows = 16;
+//
+// Rows in flight: kLaneBytesInFlight bytes per lane (4 rows of 512 bytes, 8 of
+// 256), which keeps a thread within 64 registers, so that 4 CTAs of 8 warps
+// share an SM.  Measured against 16 rows per warp at 2 CTAs per SM: the
+// lookup of the training batch (bags of 1..8) 420 -> 273 us, one-hot rows of
+// 512 bytes 297 -> 221 us, bf16 bags of 1..64 890 -> 649 us, rows of 256
+// bytes 128 -> 94 us.  The warps, not the bytes each keeps moving, hide the
+// latency of the lookups' dependent steps (offsets, index, row).
+constexpr int kLaneBytesInFlight = 64;
+constexpr int kListMinBlocks = 4;
 
 template <int BYTES>
 struct Piece;
@@ -193,11 +202,11 @@ struct ListShape {
 };
 
 template <int D, typename TE, typename TI>
-__global__ void __launch_bounds__(kBagThreads, 2) embbag_list_kernel(const __grid_constant__ FwdArgs a)
+__global__ void __launch_bounds__(kBagThreads, kListMinBlocks) embbag_list_kernel(const __grid_constant__ FwdArgs a)
 {
     using S = ListShape<D, TE>;
     constexpr int NP = S::kPieces, NE = S::kElems, PB = S::kPieceBytes;
-    constexpr int R = NP > 1 ? kRows / 2 : kRows;  // rows in flight: the same bytes per lane for two-piece rows
+    constexpr int R = kLaneBytesInFlight / (NP * PB) > 0 ? kLaneBytesInFlight / (NP * PB) : 1;  // rows in flight
     using PieceT = Piece<PB>;
     const int lane = threadIdx.x % kWarp;
     const int64_t nbags = static_cast<int64_t>(a.T) * a.B;

@@ -80,9 +80,10 @@ __device__ __forceinline__ int64_t load_index(const void* p, int64_t i)
 }
 
 // ---------------------------------------------------------------------------
-// Pool one bag in registers into an fp32 shared-memory row (one warp).
+// Pool one bag in registers into an fp32 shared-memory row (one warp), up to
+// MAXU row-load instructions in flight.
 // ---------------------------------------------------------------------------
-template <int D, typename TE, typename TI>
+template <int D, typename TE, typename TI, int MAXU = 16>
 __device__ void pool_bag_warp(const TE* __restrict__ table, int64_t V_t, const void* indices, int64_t start,
                               int L, bool mean, float* vrow, int lane, int32_t* status)
 {
@@ -91,7 +92,7 @@ __device__ void pool_bag_warp(const TE* __restrict__ table, int64_t V_t, const v
     constexpr int LPR = CPR < kWarp ? CPR : kWarp;  // lanes per row
     constexpr int CPL = CPR / LPR;               // chunks per lane
     constexpr int RPI = kWarp / LPR;             // rows per load instruction
-    constexpr int U0 = (kWarp / RPI) < 16 ? (kWarp / RPI) : 16;
+    constexpr int U0 = (kWarp / RPI) < MAXU ? (kWarp / RPI) : MAXU;
     constexpr int U = (U0 / CPL) > 0 ? (U0 / CPL) : 1;  // load instructions in flight
     constexpr int STEP = RPI * U;                // lookups per step (divides 32)
     static_assert(kWarp % STEP == 0, "step must divide the warp");
@@ -246,8 +247,17 @@ __device__ void gram_upper(const float* __restrict__ V, const GroupLayout& g, fl
 // ---------------------------------------------------------------------------
 // The forward kernel.
 // ---------------------------------------------------------------------------
+// Samples of long bags (G = 2 warps each) keep 8 row loads in flight per warp within 85 registers, so that
+// 12 of their CTAs (of 64 threads) share an SM instead of 8: workload 3 (bf16 bags of 1..64) 743.5 -> 616.7 us
+// against 16 loads in flight per warp.  More warps, not more loads per warp, hide the lookups' latency.
+template <int G>
+constexpr int ffma_min_blocks() { return G == 2 ? 3 : 1; }
+template <int G>
+constexpr int ffma_loads_in_flight() { return G == 2 ? 8 : 16; }
+
 template <int D, typename TE, typename TI, int MODE, int G>
-__global__ void __launch_bounds__(256) forward_kernel(const __grid_constant__ FwdArgs a, int groups_per_cta)
+__global__ void __launch_bounds__(256, ffma_min_blocks<G>()) forward_kernel(const __grid_constant__ FwdArgs a,
+                                                                           int groups_per_cta)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int GT = G * kWarp;
@@ -342,7 +352,8 @@ __global__ void __launch_bounds__(256) forward_kernel(const __grid_constant__ Fw
         for (int t = wig; t < T; t += G) {
             const int len = lens[t + 1];
             if (len < 0) continue;
-            pool_bag_warp<D, TE, TI>(static_cast<const TE*>(a.tables[t]), a.num_rows[t], a.indices, slot[t + 1],
+            pool_bag_warp<D, TE, TI, ffma_loads_in_flight<G>()>(static_cast<const TE*>(a.tables[t]), a.num_rows[t],
+                                                                a.indices, slot[t + 1],
                                      len, a.mean != 0, V + (t + 1) * S, lane, a.status);
         }
     }
