@@ -122,7 +122,12 @@ dlrm_status dlrm_interact_fwd(const float *dense, const float *pooled,
  * in one pass; the pooled vectors stay on chip.  Same result as
  * dlrm_embbag_fwd followed by dlrm_interact_fwd.
  * dense: device B x D; out: device B x (D+N(N-1)/2); pooled_save: device
- * B x T x D or NULL (written when given, for the training step). */
+ * B x T x D or NULL (written when given, for the training step).  With
+ * pooled_save given, bags of more than 1.25 lookups on average are pooled by
+ * the lookup kernel into pooled_save and the interaction reads them back (two
+ * kernels, the same values), which is faster for such bags than pooling on
+ * chip; an inference caller with the memory to spare may pass a scratch
+ * buffer here for that reason. */
 dlrm_status dlrm_sparse_fwd(const dlrm_tables *tables, const dlrm_bags *bags,
                             dlrm_pool_mode mode, const float *dense,
                             float *out, float *pooled_save,
