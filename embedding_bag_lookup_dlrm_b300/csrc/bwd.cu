@@ -118,6 +118,27 @@ __host__ __device__ inline BwdLayout make_bwd_layout(int T, int D)
     return l;
 }
 
+// NQ row pairs of a block of dV at one lane's 4 columns, summed over j in
+// increasing order: p[q][c] += (g(i0+2q, j), g(i0+2q+1, j)) * V[j][col+c],
+// with v pointing at V[0][col] and g at column i0 of row 0 of g.
+template <int NQ>
+__device__ __forceinline__ void grad_rows(const float* v, const float* g, int N, int NP, int D, float2 (&p)[4][4])
+{
+    for (int j = 0; j < N; ++j) {
+        const float4 vj = *reinterpret_cast<const float4*>(v + j * D);
+        const float4 g0 = *reinterpret_cast<const float4*>(g + j * NP);
+        const float4 g1 = NQ > 2 ? *reinterpret_cast<const float4*>(g + j * NP + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float2 gq[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w), make_float2(g1.x, g1.y),
+                              make_float2(g1.z, g1.w)};
+        const float2 vv[4] = {make_float2(vj.x, vj.x), make_float2(vj.y, vj.y), make_float2(vj.z, vj.z),
+                              make_float2(vj.w, vj.w)};
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) p[q][c4] = __ffma2_rn(gq[q], vv[c4], p[q][c4]);
+    }
+}
+
 // In mean mode dP[b][t] is stored already divided by the bag length L (the
 // scale every lookup of the bag applies), so the per-row sums are plain sums.
 template <int D, int G, typename TI>
@@ -200,19 +221,16 @@ __global__ void __launch_bounds__(G == 1 ? 128 : G * kWarp, G == 4 ? 9 : 1) inte
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) p[q][c4] = make_float2(0.f, 0.f);
-            for (int j = 0; j < N; ++j) {
-                const float4 v = *reinterpret_cast<const float4*>(V + j * D + col);
-                const float4 g0 = *reinterpret_cast<const float4*>(gm + j * NP + i0);
-                const float4 g1 = *reinterpret_cast<const float4*>(gm + j * NP + i0 + 4);
-                const float2 gq[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w), make_float2(g1.x, g1.y),
-                                      make_float2(g1.z, g1.w)};
-                const float2 vv[4] = {make_float2(v.x, v.x), make_float2(v.y, v.y), make_float2(v.z, v.z),
-                                      make_float2(v.w, v.w)};
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) p[q][c4] = __ffma2_rn(gq[q], vv[c4], p[q][c4]);
-            }
+            // only the row pairs that hold a row of V: the last block of N = 27 has 2 of its 4
+            const int nq = min(4, (N - i0 + 1) / 2);
+            if (nq == 4)
+                grad_rows<4>(V + col, gm + i0, N, NP, D, p);
+            else if (nq == 3)
+                grad_rows<3>(V + col, gm + i0, N, NP, D, p);
+            else if (nq == 2)
+                grad_rows<2>(V + col, gm + i0, N, NP, D, p);
+            else
+                grad_rows<1>(V + col, gm + i0, N, NP, D, p);
             float4 acc[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
