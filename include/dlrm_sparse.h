@@ -226,23 +226,22 @@ dlrm_status dlrm_sparse_bwd_update(const dlrm_tables *tables, const dlrm_bags *b
  * dlrm_sparse_bwd_sort builds the lookup keys (global row id, dP row) of the
  * bags and sorts them stably by row into `workspace` (at least
  * dlrm_sparse_bwd_workspace_size() bytes, 16-byte aligned), on `stream`.  It
- * reads only the bags and the tables' row counts (tables->data is not read,
- * dtype must be DLRM_F32); out-of-range indices and malformed offsets are
- * flagged in status_dev as in the forward.
+ * reads only the bags and the tables' row counts (the tables' device memory
+ * is not read; dtype must be DLRM_F32); out-of-range indices and malformed
+ * offsets are flagged in status_dev as in the forward.
  *
  * dlrm_sparse_bwd_update_sorted is dlrm_sparse_bwd_update (arguments, limits,
  * errors, results bit for bit) minus the key build and the sort: it reads the
  * sorted lookups that dlrm_sparse_bwd_sort left in the same workspace.
- * sorted: optional event recorded on the sort's stream after the sort; the
- * call queues the interaction backward (which does not read the sorted
- * lookups), then makes `stream` wait for `sorted`, then queues the per-row
- * sums.  NULL: the caller has ordered the sort before the call (same stream,
- * or its own event wait).  The sort itself must be queued before this call,
- * and nothing else may write the workspace in between (the sort writes only
- * the key and value parts, the interaction backward only the dP part, so the
- * two may run at the same time).  Bags,
- * tables' row counts and workspace must be those of the sort; other bags give
- * wrong row updates, not an error. */
+ * sorted: optional event, recorded on the sort's stream after the sort and
+ * before this call; the call queues the interaction backward (which does not
+ * read the sorted lookups), then makes `stream` wait for `sorted`, then
+ * queues the per-row sums.  NULL: the caller has ordered the sort before the
+ * call (same stream, or its own event wait).  Nothing else may write the
+ * workspace between the two calls (the sort writes only its key and value
+ * parts, the interaction backward only the dP part, so those two may run at
+ * the same time).  Bags, tables' row counts and workspace must be those of
+ * the sort; other bags give wrong row updates, not an error. */
 dlrm_status dlrm_sparse_bwd_sort(const dlrm_tables *tables, const dlrm_bags *bags,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *status_dev, cudaStream_t stream);
