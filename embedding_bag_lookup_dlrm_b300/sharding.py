@@ -230,19 +230,19 @@ class ShardedSparse:
         N = p.T + 1
         if out is None:
             out = self.torch.empty((p.B, p.D + N * (N - 1) // 2), dtype=self.torch.float32, device=self.dev)
-        for g in range(p.G):
-            if self.shard_tables[g] is not None:
-                idx, off = shard_bags[g]
-                dlrm_embbag_fwd(self.shard_tables[g], idx, off, mode, pooled=self.by_table[g], stream=stream)
+        def lookup(g, s):
+            idx, off = shard_bags[g]
+            dlrm_embbag_fwd(self.shard_tables[g], idx, off, mode, pooled=self.by_table[g], stream=s)
+        self._side_by_side([g for g in range(p.G) if self.shard_tables[g] is not None], lookup, stream)
         if after:
             after("lookup")
         self._exchange(1, self.by_table, self.by_sample, stream)
         if after:
             after("exchange")
-        for h in range(p.H):
+        def interact(h, s):
             lo, hi = p.samples_of(h)
-            if hi > lo:
-                dlrm_interact_fwd(dense[lo:hi], self.by_sample[h], out=out[lo:hi], stream=stream)
+            dlrm_interact_fwd(dense[lo:hi], self.by_sample[h], out=out[lo:hi], stream=s)
+        self._side_by_side([h for h in range(p.H) if p.samples_of(h)[1] > p.samples_of(h)[0]], interact, stream)
         if after:
             after("interaction")
         return out
@@ -259,42 +259,52 @@ class ShardedSparse:
         if not hasattr(self, "grad_sample"):
             self.grad_sample = [self.torch.empty_like(x) for x in self.by_sample]
             self.grad_table = [self.torch.empty_like(x) for x in self.by_table]
-        for h in range(p.H):
+        def interact_bwd(h, s):
             lo, hi = p.samples_of(h)
-            if hi > lo:
-                dlrm_interact_bwd(dense[lo:hi], self.by_sample[h], grad_out[lo:hi], grad_dense=grad_dense[lo:hi],
-                                  grad_pooled=self.grad_sample[h], stream=stream)
+            dlrm_interact_bwd(dense[lo:hi], self.by_sample[h], grad_out[lo:hi], grad_dense=grad_dense[lo:hi],
+                              grad_pooled=self.grad_sample[h], stream=s)
+        self._side_by_side([h for h in range(p.H) if p.samples_of(h)[1] > p.samples_of(h)[0]], interact_bwd, stream)
         if after:
             after("interaction_bwd")
         self._exchange(0, self.grad_table, self.grad_sample, stream)
         if after:
             after("exchange_bwd")
-        # the table shards update disjoint tables from separate workspaces: on one device they run side by
-        # side, each on a stream of its own forked from the caller's stream and joined back to it
-        main = stream if stream is not None else self.torch.cuda.current_stream(self.dev)
-        if not hasattr(self, "_upd_streams"):
-            self._upd_streams = [self.torch.cuda.Stream(device=self.dev) for _ in range(p.G)]
-        fork = self.torch.cuda.Event()
-        fork.record(main)
-        joins = []
-        for g in range(p.G):
-            if self.shard_tables[g] is None:
-                continue
+        # the table shards update disjoint tables from separate workspaces
+        def update(g, s):
             idx, off = shard_bags[g]
             acc = [accum[t] for t in p.tables_of(g)] if accum is not None else None
             ws = self._workspace(g, idx, off, mode)
-            us = self._upd_streams[g]
-            us.wait_event(fork)
             dlrm_embbag_bwd_update(self.shard_tables[g], idx, off, self.grad_table[g], rule, lr, eps, acc, mode,
-                                   workspace=ws, stream=us)
-            ev = self.torch.cuda.Event()
-            ev.record(us)
-            joins.append(ev)
-        for ev in joins:
-            main.wait_event(ev)
+                                   workspace=ws, stream=s)
+        self._side_by_side([g for g in range(p.G) if self.shard_tables[g] is not None], update, stream)
         if after:
             after("update")
         return grad_dense
+
+    def _side_by_side(self, shards, fn, stream=None):
+        """fn(shard, s) for every shard, each on a stream of its own forked from the caller's stream and
+        joined back to it: the shards' work is independent (each writes its own buffers), so on one device
+        the shards run side by side as they would on devices of their own."""
+        main = stream if stream is not None else self.torch.cuda.current_stream(self.dev)
+        if len(shards) <= 1:
+            for k in shards:
+                fn(k, main)
+            return
+        if not hasattr(self, "_streams"):
+            self._streams = []
+        while len(self._streams) < len(shards):
+            self._streams.append(self.torch.cuda.Stream(device=self.dev))
+        fork = self.torch.cuda.Event()
+        fork.record(main)
+        joins = []
+        for k, s in zip(shards, self._streams):
+            s.wait_event(fork)
+            fn(k, s)
+            ev = self.torch.cuda.Event()
+            ev.record(s)
+            joins.append(ev)
+        for ev in joins:
+            main.wait_event(ev)
 
     def _workspace(self, g, idx, off, mode):
         """A workspace per table shard, grown when a batch needs more (allocated outside any timed step
