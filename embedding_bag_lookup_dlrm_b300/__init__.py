@@ -100,7 +100,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                     P], i32),
         "dlrm_sparse_bwd_sort": ([T, B, P, ctypes.c_size_t, P, P], i32),
         "dlrm_sparse_bwd_update_sorted": ([T, B, i32, P, P, P, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t,
-                                           P, P, P], i32),
+                                           P, P, P, P], i32),
         "dlrm_interact_bwd": ([P, P, P, i64, i32, i32, P, P, P], i32),
         "dlrm_embbag_bwd_workspace_size": ([T, B, i32, ctypes.POINTER(ctypes.c_size_t)], i32),
         "dlrm_embbag_bwd_update": ([T, B, i32, P, ctypes.POINTER(DlrmUpdate), P, ctypes.c_size_t, P, P, P], i32),
@@ -456,10 +456,12 @@ def dlrm_sparse_bwd_sort(tables, indices, offsets, workspace, status=None, strea
 
 def dlrm_sparse_bwd_update_sorted(tables, indices, offsets, dense, pooled_saved, grad_out, rule, lr, eps=0.0,
                                   accum=None, mode="sum", grad_dense=None, workspace=None, status=None, sorted=None,
-                                  stream=None):
+                                  grad_ready=None, stream=None):
     """dlrm_sparse_bwd_update on a workspace that dlrm_sparse_bwd_sort filled for the same bags (queued
     before this call).  sorted: a torch.cuda.Event recorded after the sort on its stream, waited for before
-    the per-row sums only (None: the caller ordered the sort before this call).  Returns grad_dense [B, D]."""
+    the per-row sums only (None: the caller ordered the sort before this call).  grad_ready: a
+    torch.cuda.Event the call records once grad_dense is queued, before the per-row sums.  Returns
+    grad_dense [B, D]."""
     lib = load_library()
     tb = _tables(tables)
     B = _batch(offsets, tb.T)
@@ -479,6 +481,7 @@ def dlrm_sparse_bwd_update_sorted(tables, indices, offsets, dense, pooled_saved,
                                                grad_dense.data_ptr(), ctypes.byref(upd), workspace.data_ptr(),
                                                workspace.numel(), status.data_ptr() if status is not None else None,
                                                sorted.cuda_event if sorted is not None else None,
+                                               grad_ready.cuda_event if grad_ready is not None else None,
                                                _stream_ptr(stream, dev))
     _raise(st, "dlrm_sparse_bwd_update_sorted")
     return grad_dense
@@ -772,10 +775,32 @@ class DLRMModel:
             self._buf[key] = t
         return t
 
-    def forward(self, dense_in, indices, offsets, mode="sum", stream=None, after=None, before_sparse=None):
+    def forward(self, dense_in, indices, offsets, mode="sum", stream=None, after=None, lookup_stream=None,
+                after_lookup=None):
         """Bottom MLP, sparse forward (pooled vectors saved), top MLP; returns the top MLP's output.
-        before_sparse: called once the bottom MLP is queued, before the sparse forward."""
+        lookup_stream: forked from the caller's stream at the start; bags of more than 1.25 lookups on average
+        are pooled there (dlrm_embbag_fwd) beside the bottom MLP, since the lookup needs only the bags, and the
+        interaction (dlrm_interact_fwd) follows the bottom MLP; after_lookup() is called once that is queued,
+        to queue more work on lookup_stream.  Otherwise the fused forward (dlrm_sparse_fwd) follows the bottom
+        MLP.  Both give the same values: dlrm_sparse_fwd with pooled vectors saved runs those two kernels for
+        such bags."""
         B = dense_in.shape[0]
+        N = self.tables.T + 1
+        out = self._get("out", (B, self.tables.D + N * (N - 1) // 2))
+        pooled = self._get("pooled", (B, self.tables.T, self.tables.D))
+        main = stream if stream is not None else torch.cuda.current_stream(dense_in.device)
+        split = lookup_stream is not None and 4 * indices.numel() > 5 * self.tables.T * B
+        lookup_ev = None
+        if lookup_stream is not None:
+            fork = torch.cuda.Event()
+            fork.record(main)
+            lookup_stream.wait_event(fork)
+            if split:
+                dlrm_embbag_fwd(self.tables, indices, offsets, mode, pooled=pooled, stream=lookup_stream)
+                lookup_ev = torch.cuda.Event()
+                lookup_ev.record(lookup_stream)
+            if after_lookup:
+                after_lookup()
         h = dense_in
         self.bot_in = [h]
         for i, (w, b) in enumerate(self.bottom):
@@ -786,12 +811,11 @@ class DLRMModel:
         if after:
             after("bottom_fwd")
         x = h
-        N = self.tables.T + 1
-        out = self._get("out", (B, self.tables.D + N * (N - 1) // 2))
-        pooled = self._get("pooled", (B, self.tables.T, self.tables.D))
-        if before_sparse:
-            before_sparse()
-        dlrm_sparse_fwd(self.tables, indices, offsets, x, mode, out=out, pooled_save=pooled, stream=stream)
+        if split:
+            main.wait_event(lookup_ev)
+            dlrm_interact_fwd(x, pooled, out=out, stream=stream)
+        else:
+            dlrm_sparse_fwd(self.tables, indices, offsets, x, mode, out=out, pooled_save=pooled, stream=stream)
         if after:
             after("sparse_fwd")
         g = out
@@ -807,23 +831,24 @@ class DLRMModel:
 
     def train_step(self, dense_in, indices, offsets, label, lr_mlp, lr_emb, eps=1e-8, accum=None, rule="adagrad",
                    mode="sum", stream=None, side_stream=None, after=None):
-        """One training step; returns (loss [1], prob [B]) as device tensors.  With side_stream the lookup-key
-        build and sort of the sparse backward run there (they depend only on the bags), from the sparse
-        forward on, beside everything up to the sparse backward's per-row sums (the bottom MLP's short GEMMs,
-        which the sort's blocks would delay, run before it); without it they run inside the sparse backward."""
+        """One training step; returns (loss [1], prob [B]) as device tensors.
+
+        With side_stream, the work that depends only on the bags runs there from the step's start: the lookup of
+        multi-lookup bags beside the bottom MLP, then the lookup-key build and sort of the sparse backward beside
+        the rest of the forward; and the bottom MLP's backward, which needs only grad_x, runs on a stream of the
+        model's own beside the sparse backward's per-row sums.  Without it every step runs on the caller's stream
+        (the sort inside the sparse backward)."""
         B = dense_in.shape[0]
         ws = self._ws("ws_sparse", dlrm_sparse_bwd_workspace_size(self.tables, indices, offsets))
+        main = stream if stream is not None else torch.cuda.current_stream(dense_in.device)
         sorted_ev = torch.cuda.Event() if side_stream is not None else None
 
         def sort_beside():
-            fork = torch.cuda.Event()
-            fork.record(stream if stream is not None else torch.cuda.current_stream(dense_in.device))
-            side_stream.wait_event(fork)
             dlrm_sparse_bwd_sort(self.tables, indices, offsets, ws, stream=side_stream)
             sorted_ev.record(side_stream)
 
-        g = self.forward(dense_in, indices, offsets, mode, stream, after,
-                         before_sparse=sort_beside if side_stream is not None else None)
+        g = self.forward(dense_in, indices, offsets, mode, stream, after, lookup_stream=side_stream,
+                         after_lookup=sort_beside if side_stream is not None else None)
         w, b = self.head
         prob, loss, dh = dlrm_head_bce_sgd(g, w, b, label, lr_mlp, prob=self._get("prob", (B,)),
                                            loss=self._get("loss", (1,)), dh=self._get("dh", (B, w.shape[0])),
@@ -841,10 +866,16 @@ class DLRMModel:
             after("top_bwd")
         x = self.bot_in[-1]
         gx = self._get("grad_x", (B, self.tables.D))
+        bottom_stream = main
         if sorted_ev is not None:
+            gx_ready = torch.cuda.Event()
             dlrm_sparse_bwd_update_sorted(self.tables, indices, offsets, x, self._buf["pooled"], dy, rule, lr_emb,
                                           eps, accum, mode, grad_dense=gx, workspace=ws, sorted=sorted_ev,
-                                          stream=stream)
+                                          grad_ready=gx_ready, stream=stream)
+            if "bwd_stream" not in self._buf:
+                self._buf["bwd_stream"] = torch.cuda.Stream(device=dense_in.device)
+            bottom_stream = self._buf["bwd_stream"]
+            bottom_stream.wait_event(gx_ready)
         else:
             dlrm_sparse_bwd_update(self.tables, indices, offsets, x, self._buf["pooled"], dy, rule, lr_emb, eps,
                                    accum, mode, grad_dense=gx, workspace=ws, stream=stream)
@@ -857,7 +888,11 @@ class DLRMModel:
             dy = dlrm_fc_bwd_sgd(xin, W, bb, yout, dy, lr_mlp, True,
                                  dx=self._get(("dbot", i), tuple(xin.shape)) if i > 0 else None, want_dx=i > 0,
                                  workspace=self._ws(("ws_bot", i), fc_bwd_workspace_size(B, W.shape[1], W.shape[0])),
-                                 stream=stream)
+                                 stream=bottom_stream)
+        if bottom_stream is not main:
+            done = torch.cuda.Event()
+            done.record(bottom_stream)
+            main.wait_event(done)
         if after:
             after("bottom_bwd")
         return loss, prob

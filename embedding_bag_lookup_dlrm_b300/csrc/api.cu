@@ -255,7 +255,7 @@ dlrm_status pack_update(BwdArgs& a, const dlrm_tables* tables, const dlrm_bags* 
 dlrm_status sparse_bwd(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode, const float* dense,
                        const float* pooled_saved, const float* grad_out, float* grad_dense, const dlrm_update* update,
                        void* workspace, size_t workspace_bytes, int32_t* status_dev, cudaStream_t stream,
-                       cudaStream_t side_stream, bool presorted, cudaEvent_t sorted)
+                       cudaStream_t side_stream, bool presorted, cudaEvent_t sorted, cudaEvent_t grad_ready)
 {
     BwdArgs a;
     dlrm_status st = pack_update(a, tables, bags, mode, update, workspace, status_dev);
@@ -273,7 +273,7 @@ dlrm_status sparse_bwd(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_po
     a.grad_out = grad_out;
     a.grad_dense = grad_dense;
     return dlrm::launch_backward(a, tables->dim, bags->index_type, dlrm::kFromInteraction, nullptr, workspace,
-                                 workspace_bytes, stream, side_stream, presorted, sorted);
+                                 workspace_bytes, stream, side_stream, presorted, sorted, grad_ready);
 }
 
 }  // namespace
@@ -287,7 +287,7 @@ dlrm_status dlrm_sparse_bwd_update(const dlrm_tables* tables, const dlrm_bags* b
                                    cudaStream_t side_stream)
 {
     return sparse_bwd(tables, bags, mode, dense, pooled_saved, grad_out, grad_dense, update, workspace,
-                      workspace_bytes, status_dev, stream, side_stream, false, nullptr);
+                      workspace_bytes, status_dev, stream, side_stream, false, nullptr, nullptr);
 }
 
 dlrm_status dlrm_sparse_bwd_sort(const dlrm_tables* tables, const dlrm_bags* bags, void* workspace,
@@ -310,10 +310,10 @@ dlrm_status dlrm_sparse_bwd_update_sorted(const dlrm_tables* tables, const dlrm_
                                           const float* dense, const float* pooled_saved, const float* grad_out,
                                           float* grad_dense, const dlrm_update* update, void* workspace,
                                           size_t workspace_bytes, int32_t* status_dev, cudaEvent_t sorted,
-                                          cudaStream_t stream)
+                                          cudaEvent_t grad_ready, cudaStream_t stream)
 {
     return sparse_bwd(tables, bags, mode, dense, pooled_saved, grad_out, grad_dense, update, workspace,
-                      workspace_bytes, status_dev, stream, nullptr, true, sorted);
+                      workspace_bytes, status_dev, stream, nullptr, true, sorted, grad_ready);
 }
 
 dlrm_status dlrm_sparse_bwd_adagrad(const dlrm_tables* tables, const dlrm_bags* bags, dlrm_pool_mode mode,

@@ -1015,9 +1015,10 @@ dlrm_status launch_interact_bwd_groups(const BwdArgs& a, float* dP, cudaStream_t
 // bag lengths in mean mode) or the row update from a given pooled gradient (kFromPooledGrad).
 // presorted: the workspace holds the sorted pairs of these bags (sort_keys queued earlier by the caller),
 // so only the dP rows and the per-row sums run here; the per-row sums wait for `sorted` when it is given.
+// grad_ready, if given, is recorded on s once the interaction backward (grad_dense, dP) is queued.
 template <int D, typename TI>
 dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const float* grad_pooled, cudaStream_t s,
-                         cudaStream_t side, bool presorted, cudaEvent_t sorted)
+                         cudaStream_t side, bool presorted, cudaEvent_t sorted, cudaEvent_t grad_ready)
 {
     Fork f;
     const bool two = !presorted && side != nullptr && side != s && a.nnz > 0;
@@ -1041,6 +1042,8 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const
     if (st == DLRM_OK) {
         if (source == kFromInteraction) {
             st = launch_interact_bwd_groups<D, TI>(a, w.dP, s);
+            if (st == DLRM_OK && grad_ready != nullptr && cudaEventRecord(grad_ready, s) != cudaSuccess)
+                st = DLRM_ERR_CUDA;
         } else if (a.mean && a.nnz > 0) {
             const int64_t n4 = a.B * a.T * (D / 4);
             const int64_t blocks = (n4 + 255) / 256;
@@ -1070,10 +1073,11 @@ dlrm_status run_backward(const BwdArgs& a, const Workspace& w, int source, const
 
 template <int D>
 dlrm_status dispatch_bwd(const BwdArgs& a, int index_type, const Workspace& w, int source, const float* grad_pooled,
-                         cudaStream_t s, cudaStream_t side, bool presorted, cudaEvent_t sorted)
+                         cudaStream_t s, cudaStream_t side, bool presorted, cudaEvent_t sorted, cudaEvent_t grad_ready)
 {
-    return index_type == DLRM_I32 ? run_backward<D, int32_t>(a, w, source, grad_pooled, s, side, presorted, sorted)
-                                  : run_backward<D, int64_t>(a, w, source, grad_pooled, s, side, presorted, sorted);
+    return index_type == DLRM_I32
+               ? run_backward<D, int32_t>(a, w, source, grad_pooled, s, side, presorted, sorted, grad_ready)
+               : run_backward<D, int64_t>(a, w, source, grad_pooled, s, side, presorted, sorted, grad_ready);
 }
 
 bool with_dP(int source, bool mean) { return source == kFromInteraction || mean; }
@@ -1089,17 +1093,17 @@ size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz, int sou
 
 dlrm_status launch_backward(const BwdArgs& a, int dim, int index_type, int source, const float* grad_pooled,
                             void* workspace, size_t workspace_bytes, cudaStream_t s, cudaStream_t side, bool presorted,
-                            cudaEvent_t sorted)
+                            cudaEvent_t sorted, cudaEvent_t grad_ready)
 {
     size_t need = 0;
     const Workspace w = carve(workspace, a.B, a.T, dim, a.nnz, with_dP(source, a.mean != 0), &need);
     if (workspace_bytes < need) return DLRM_ERR_INVALID_ARG;
     switch (dim) {
-        case 16: return dispatch_bwd<16>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
-        case 32: return dispatch_bwd<32>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
-        case 64: return dispatch_bwd<64>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
-        case 128: return dispatch_bwd<128>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
-        case 256: return dispatch_bwd<256>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted);
+        case 16: return dispatch_bwd<16>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted, grad_ready);
+        case 32: return dispatch_bwd<32>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted, grad_ready);
+        case 64: return dispatch_bwd<64>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted, grad_ready);
+        case 128: return dispatch_bwd<128>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted, grad_ready);
+        case 256: return dispatch_bwd<256>(a, index_type, w, source, grad_pooled, s, side, presorted, sorted, grad_ready);
         default: return DLRM_ERR_UNSUPPORTED;
     }
 }

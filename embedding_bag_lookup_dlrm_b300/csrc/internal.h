@@ -90,10 +90,11 @@ size_t bwd_workspace_bytes(int64_t B, int32_t T, int32_t D, int64_t nnz, int sou
 // side: a second stream for the key build and sort (nullptr or == stream: one stream).
 // grad_pooled: the source of kFromPooledGrad (ignored otherwise).
 // presorted: the workspace holds the sorted lookups of these bags from launch_sort (side is then unused);
-// sorted, if given, is an event the per-row sums wait for (the interaction backward does not).
+// sorted, if given, is an event the per-row sums wait for (the interaction backward does not); grad_ready, if
+// given, is recorded on `stream` once the interaction backward is queued.
 dlrm_status launch_backward(const BwdArgs& args, int dim, int index_type, int source, const float* grad_pooled,
                             void* workspace, size_t workspace_bytes, cudaStream_t stream, cudaStream_t side,
-                            bool presorted = false, cudaEvent_t sorted = nullptr);
+                            bool presorted = false, cudaEvent_t sorted = nullptr, cudaEvent_t grad_ready = nullptr);
 
 // The lookup keys of the bags and their stable radix sort into a training-step workspace (the layout
 // launch_backward with source kFromInteraction reads), on `stream`.

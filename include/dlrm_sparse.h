@@ -237,7 +237,10 @@ dlrm_status dlrm_sparse_bwd_update(const dlrm_tables *tables, const dlrm_bags *b
  * before this call; the call queues the interaction backward (which does not
  * read the sorted lookups), then makes `stream` wait for `sorted`, then
  * queues the per-row sums.  NULL: the caller has ordered the sort before the
- * call (same stream, or its own event wait).  Nothing else may write the
+ * call (same stream, or its own event wait).  grad_ready: optional event the
+ * call records on `stream` right after the interaction backward, so that
+ * work needing only grad_dense (the bottom MLP's backward) can run on
+ * another stream beside the per-row sums.  Nothing else may write the
  * workspace between the two calls (the sort writes only its key and value
  * parts, the interaction backward only the dP part, so those two may run at
  * the same time).  Bags, tables' row counts and workspace must be those of
@@ -252,7 +255,7 @@ dlrm_status dlrm_sparse_bwd_update_sorted(const dlrm_tables *tables, const dlrm_
                                           float *grad_dense, const dlrm_update *update,
                                           void *workspace, size_t workspace_bytes,
                                           int32_t *status_dev, cudaEvent_t sorted,
-                                          cudaStream_t stream);
+                                          cudaEvent_t grad_ready, cudaStream_t stream);
 
 /* The interaction backward alone (calculus on "DLRM", robocikowo.com,
  * "Forward pass" steps (3)-(4)): with g(i,j) = g(j,i) = grad_out[b][D + pos(i,j)],

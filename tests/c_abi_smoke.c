@@ -74,7 +74,7 @@ static int host_checks(void)
         CHECK(dlrm_sparse_bwd_update_sorted(&tb, &bags, DLRM_POOL_SUM, (const float *)0x10,
                                             (const float *)0x10, (const float *)0x10, (float *)0x10,
                                             &upd, (void *)0x10, (size_t)1 << 62, NULL,
-                                            (cudaEvent_t)0, 0) == DLRM_ERR_INVALID_ARG);
+                                            (cudaEvent_t)0, (cudaEvent_t)0, 0) == DLRM_ERR_INVALID_ARG);
     }
     {
         int32_t shard[2] = {0, 0}, slot[2] = {0, 0}; /* slot 0 twice: inconsistent */

@@ -124,7 +124,7 @@ def test_split_step_host_checks(lib):
     acc = (ctypes.c_void_p * 2)(0x10, 0x10)
     upd = dl.DlrmUpdate(0, 0.01, 1e-8, ctypes.cast(acc, ctypes.POINTER(ctypes.c_void_p)))
     args = (ctypes.byref(tb), ctypes.byref(bags), 0, 0x10, 0x10, 0x10, 0x10, ctypes.byref(upd), 0x10, 1 << 62,
-            None, None, None)
+            None, None, None, None)
     assert lib.dlrm_sparse_bwd_update_sorted(*args) == dl.DLRM_ERR_UNSUPPORTED  # nnz = 2^32
     bags.nnz = 8
     upd.rule = 9
