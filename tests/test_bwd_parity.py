@@ -177,6 +177,35 @@ def test_sort_beside_forward_matches_one_call(mode, itype, rule, V, wait):
         assert torch.equal(a, b)
 
 
+def test_grad_ready_event_orders_grad_dense():
+    """dlrm_sparse_bwd_update_sorted's grad_ready event: a copy of grad_dense queued on another stream after
+    waiting for it (while the per-row sums still run on the call's stream) holds the final grad_dense."""
+    B, T, D = 3000, 26, 128
+    tabs, Vs, idx, off, dense = random_case(61, B, T, D, 2000, 1, 8, value_scale=0.05)
+    g = torch.from_numpy(np.random.default_rng(7).standard_normal((B, D + 27 * 13)).astype(np.float32)).cuda()
+    di, do, dx = dev_index(idx, "i32"), dev_index(off, "i32"), torch.from_numpy(dense).cuda()
+    dt = dev_tables(tabs, "f32")
+    acc = [torch.full((v,), 0.1, device="cuda") for v in Vs]
+    ps = torch.empty((B, T, D), device="cuda")
+    dl.dlrm_sparse_fwd(dt, di, do, dx, pooled_save=ps)
+    ref = dl.dlrm_interact_bwd(dx, ps, g)[0]  # grad_dense alone
+    ws = torch.empty(dl.dlrm_sparse_bwd_workspace_size(dt, di, do), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    main, other = torch.cuda.Stream(), torch.cuda.Stream()
+    gd = torch.full((B, D), float("nan"), device="cuda")
+    copy = torch.empty_like(gd)
+    ready = torch.cuda.Event()
+    with torch.cuda.stream(main):
+        dl.dlrm_sparse_bwd_sort(dt, di, do, ws, stream=main)
+        dl.dlrm_sparse_bwd_update_sorted(dt, di, do, dx, ps, g, "adagrad", 0.01, 1e-8, acc, grad_dense=gd,
+                                         workspace=ws, grad_ready=ready, stream=main)
+    other.wait_event(ready)
+    with torch.cuda.stream(other):
+        copy.copy_(gd)
+    torch.cuda.synchronize()
+    assert torch.equal(copy, ref) and torch.equal(gd, ref)
+
+
 def test_bwd_flags_bad_index(orc):
     B, T, D, V = 50, 3, 64, 30
     tabs, Vs, idx, off, dense = random_case(41, B, T, D, V, 1, 3, value_scale=0.05)
